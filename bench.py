@@ -1,0 +1,389 @@
+"""Benchmark of the paged-attention hot path on GB300.
+
+One step is one full ``attn_decode_paged`` call (paged decode kernel plus split
+merge) over the Llama-2-7B-shaped batch: bf16, batch 16, 32 query heads = 32
+KV heads, head_dim 128, KV lengths U[512, 4096], page 16, 8192-page pool. The
+metric is HBM GB/s of algorithmic bytes: each sequence's K and V read once.
+The same JSON line carries the causal prefill figure (bf16, batch 8, T 1024,
+32 heads, d 128) in TFLOP/s of causal FLOPs.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``.
+With N > 1 it runs under torchrun, one replica per GPU (the path shards by
+sequence with no exchange). Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU baseline (the fp64 oracle) runs on one host core: pin BLAS threads before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn HBM GB/s (% of peak); causal prefill attn TFLOP/s (% peak)"
+WORKLOAD = ("llama7b_batched_decode: bf16, batch 16, 32 query heads = 32 KV heads, head_dim 128, "
+            "kv_len U[512,4096] seeded, page_size 16, 8192-page pool, one query token per sequence")
+PREFILL_WORKLOAD = "causal_prefill_llama7b: bf16, batch 8, T 1024, 32/32 heads, head_dim 128, [B,T,H,D]"
+FALLBACK_HBM = 6800.0
+FALLBACK_BF16 = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM, FALLBACK_BF16, 1700.0, "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_28_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, src_hash, units_now):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this exact source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel_key)
+    if not d or d.get("source_hash") != src_hash:
+        return None
+    return d["dram_bytes_per_launch"] * units_now / d["units"]
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.seek(0)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_decode_rate(case, budget_s=12.0):
+    """Times the fp64 oracle, as it stands, on whole passes over the decode batch until
+    ``budget_s`` has elapsed. Returns (GB/s of algorithmic bytes, passes, seconds)."""
+    import oracle
+    q = case.q.double().numpy()
+    kp = case.k_pages.float().numpy()
+    vp = case.v_pages.float().numpy()
+    bt = case.block_table.numpy()
+    lens = case.kv_lens.numpy()
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_paged(q, kp, vp, bt, lens, case.scale)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return case.kv_bytes() * passes / el / 1e9, passes, el
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host cores: the reference arm of this benchmark."""
+    if rank != 0:
+        return
+    from paged_kv_attention_28_gb300 import workloads
+    case = workloads.llama7b_batched_decode(poison=False)
+    for _ in range(args.warmup):
+        pass
+    rates, secs = [], []
+    per_step = max(1.0, 10.0 / max(1, args.steps))
+    for _ in range(args.steps):
+        r, passes, el = oracle_decode_rate(case, budget_s=per_step)
+        rates.append(r)
+        secs.append(el / passes)
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.mean(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "whole passes of the fp64 oracle over the full decode batch "
+                                   f"(~{per_step:.0f} s per step)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local):
+    from paged_kv_attention_28_gb300 import build as _b
+    if rank == 0:
+        _b.build(quiet=True)
+    barrier(world)
+    from paged_kv_attention_28_gb300 import binding as B
+    from paged_kv_attention_28_gb300 import workloads
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+
+    case = workloads.llama7b_batched_decode(poison=False)
+    cpu_rate = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_rate = oracle_decode_rate(case, budget_s=12.0)
+
+    q = case.q.to(dev)
+    kp = case.k_pages.to(dev)
+    vp = case.v_pages.to(dev)
+    bt = case.block_table.to(dev)
+    lens = case.kv_lens.to(dev)
+    B_, Hq, D = case.q.shape
+    S = B.decode_num_splits(B_, case.max_blocks, Hq, case.n_kv_heads, D, case.page_size, 0)
+    ws = B.alloc_workspace(B.decode_workspace_size(B_, case.max_blocks, Hq, case.n_kv_heads, D,
+                                                   case.page_size, 0), dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(B_, Hq, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 1 + (1 if S > 1 else 0)
+    algo_bytes = case.kv_bytes()
+
+    def step():
+        B.decode_paged(q, kp, vp, bt, lens, case.scale, num_splits=0, out=out, lse=lse,
+                       workspace=ws, err_flag=err)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))                 # evict L2 between steps (not timed)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t0
+    assert int(err.item()) == 0, f"device error flag {int(err.item())}"
+    times_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = sum(times_ms) / 1e3
+    total_s = max_over_ranks(total_s, world)
+    value = algo_bytes * args.steps * world / total_s / 1e9
+    ms_per_step = 1000 * total_s / args.steps
+    kernel_gbs = algo_bytes / (statistics.mean(times_ms) / 1e3) / 1e9
+
+    # ---- end to end through the public call: pinned host inputs in, results out, every step
+    h_q = case.q.pin_memory()
+    h_bt = case.block_table.pin_memory()
+    h_lens = case.kv_lens.pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = args.steps
+    for _ in range(2):
+        q.copy_(h_q, non_blocking=True)
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(h_q, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        lens.copy_(h_lens, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e_value = algo_bytes * e2e_steps * world / e2e_s / 1e9
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_lens))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+
+    units = int(case.kv_lens.sum())
+    traffic = profiled_traffic("decode_llama7b_batched", source_hash("decode_kernel.cuh", "decode.cu"),
+                               units)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}", "num_splits": S,
+                   "algorithmic_bytes_per_step": algo_bytes,
+                   "l2": "inputs (604 MB of K/V) exceed the 129 MB L2, and a 256 MiB buffer is written between timed steps",
+                   "timing": "CUDA events around each call on the launch stream; sum over steps; max over ranks"},
+        "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": kernel_gbs / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": traffic, "kernel": "decode_paged_kernel (+ merge_splits_kernel inside the same events)"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "q, block_table and kv_lens copied in from pinned host memory and out, lse copied back every step; the KV page pool is resident device state"},
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s": wall,
+    }
+    if cpu_rate is not None:
+        line["cpu_baseline"] = {"value": cpu_rate[0], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{cpu_rate[1]} whole pass(es) of the fp64 oracle over the same decode batch in {cpu_rate[2]:.1f} s"}
+
+    # ---- causal prefill on the same line (its own roofline against dense bf16)
+    pre = prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src)
+    if pre is not None:
+        line["prefill"] = pre
+        line["gpu_launches"] += pre.pop("launches")
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src):
+    case = workloads.causal_prefill_llama7b()
+    q, k, v = case.q.to(dev), case.k.to(dev), case.v.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(case.batch, case.n_qo_heads, case.seq_len, dtype=torch.float32, device=dev)
+    try:
+        B.prefill_causal(q, k, v, case.scale, out=out, lse=lse)
+    except B.AttnError as e:
+        if e.status == B.PKV_ERR_UNSUPPORTED:
+            return None
+        raise
+    for _ in range(max(3, args.warmup)):
+        B.prefill_causal(q, k, v, case.scale, out=out, lse=lse)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        B.prefill_causal(q, k, v, case.scale, out=out, lse=lse)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / 1e3, world)
+    flops = case.causal_flops()
+    tflops = flops * args.steps * world / t / 1e12
+    per = flops * args.steps / t / 1e12
+    return {"workload": PREFILL_WORKLOAD, "value": tflops, "unit": "TFLOP/s",
+            "ms_per_step": 1000 * t / args.steps, "causal_flops_per_step": flops,
+            "roofline": {"bound": "tensor", "achieved": per, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": per / bf16_peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "traffic": None, "kernel": "prefill_causal_kernel"},
+            "launches": args.steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,224 @@
+/*
+ * pkv_attn.h: C ABI of the GB300 (sm_103a) paged / causal attention library.
+ *
+ * Every call computes scaled-dot-product attention, softmax(Q K^T * scale) V
+ * ("FlashInfer内核库：利用CUDA Warp-Level Primitives加速级联推理的Attention计算",
+ * section 1). The score matrix is never written to memory: scores, softmax and
+ * the weighted sum of V stay on chip ("快速注意力内核与算子融合", Q&A on
+ * FlashAttention; the FMHA page "TensorRT-LLM深度优化", section 2).
+ *
+ * Conventions common to every call
+ * --------------------------------
+ * - Pointers named q, k*, v*, out*, lse*, block_table*, kv_lens*, *_lens,
+ *   workspace and err_flag are DEVICE pointers. The caller owns them. The
+ *   library never allocates, frees, copies to the host or synchronises.
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *   stream. All work is enqueued on it asynchronously. Outputs are valid once
+ *   the caller has synchronised with that stream.
+ * - Element types: PKV_F32 (float) or PKV_BF16 (bfloat16). Softmax statistics
+ *   and partial states are always fp32. Outputs are rounded to the input type
+ *   with round-to-nearest-even.
+ * - lse is the natural logarithm of sum_j exp(scale * q . k_j), in fp32. It is
+ *   -inf when there is no key; the output row is then 0.
+ * - GQA: query head h reads KV head h / (n_qo_heads / n_kv_heads).
+ *   n_qo_heads must be a multiple of n_kv_heads.
+ * - Return value: PKV_OK (0) or a negative PKV_ERR_* code. A non-zero code
+ *   means nothing was enqueued, except PKV_ERR_LAUNCH, which reports the CUDA
+ *   launch error. Arguments are checked on the host before any launch. No call
+ *   aborts the process.
+ * - err_flag (nullable, int32 in device memory) collects problems that only
+ *   the device can see, as a bitwise OR of PKV_DEVERR_* bits: a block-table
+ *   entry outside [0, num_pages), a length above the table's capacity, or a
+ *   pipeline wait that timed out. The rows affected are written as NaN. The
+ *   caller clears the flag; the library only ORs bits into it.
+ *
+ * Paged KV layout
+ * ---------------
+ *   k_pages, v_pages : [num_pages][n_kv_heads][page_size][head_dim]
+ *   block_table      : int32 [batch][max_blocks_per_seq], row-major
+ *   kv_lens          : int32 [batch]
+ * Token t of sequence b lives in physical page block_table[b][t / page_size],
+ * slot t % page_size ("快速注意力内核与算子融合", Q&A on paged attention: a block
+ * table maps logical blocks to physical blocks). Table entries at or past
+ * ceil(kv_len / page_size), and the slots of the last page past kv_len, are
+ * never read.
+ */
+#ifndef PKV_ATTN_H
+#define PKV_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types */
+#define PKV_F32 0
+#define PKV_BF16 1
+
+/* status codes */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1) /* null pointer, negative size, inconsistent shape */
+#define PKV_ERR_UNSUPPORTED (-2) /* valid but not built: head_dim, page_size, group size, dtype */
+#define PKV_ERR_WORKSPACE (-3)   /* workspace missing or smaller than the *_workspace_size call says */
+#define PKV_ERR_LAUNCH (-4)      /* a CUDA launch or attribute call failed */
+#define PKV_ERR_DEVICE (-5)      /* no usable sm_100-family device is current */
+
+/* device-side error bits ORed into *err_flag */
+#define PKV_DEVERR_BAD_PAGE 1 /* a block-table entry outside [0, num_pages) */
+#define PKV_DEVERR_BAD_LEN 2  /* a length < 0 or > max_blocks * page_size */
+#define PKV_DEVERR_TIMEOUT 4  /* a bounded pipeline wait gave up (nothing hung) */
+
+/* Support set of this build (others return PKV_ERR_UNSUPPORTED):
+ *   decode / cascade : head_dim 64 or 128; page_size 16; group size 1, 2, 4 or 8;
+ *                      PKV_F32 or PKV_BF16 (cascade: PKV_BF16, head_dim 128)
+ *   prefill          : head_dim 128; PKV_BF16; any seq_len >= 1
+ */
+
+/* Human-readable name of a status code. Static storage; never NULL. */
+const char* attn_status_string(int status);
+
+/*
+ * Number of KV splits the decode calls use for this shape. num_splits > 0 is
+ * taken as asked (capped at max_blocks_per_seq); 0 lets the library choose from
+ * the shape and the SM count of the current device. A split covers a contiguous
+ * range of ceil(max_blocks_per_seq / splits) pages of a sequence.
+ * FlashDecoding computes each partial softmax independently and combines them
+ * all at the end ("【FlashAttention-V4，非官方】FlashDecoding++", section 1).
+ * Returns the split count (>= 1) or a negative PKV_ERR_* code.
+ */
+int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, int n_kv_heads,
+                           int head_dim, int page_size, int num_splits);
+
+/*
+ * Workspace bytes attn_decode_paged and attn_decode_paged_unified_max need for
+ * this shape: the fp32 partial states O[batch][n_qo_heads][splits][head_dim] and
+ * LSE[batch][n_qo_heads][splits]. It is 0 when one split suffices. Returns
+ * (size_t)-1 for invalid arguments.
+ */
+size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_splits);
+
+/*
+ * Single-token decode over a paged KV cache.
+ *
+ *   q     : [batch][n_qo_heads][head_dim], dtype
+ *   out   : [batch][n_qo_heads][head_dim], dtype (must not alias an input)
+ *   lse   : [batch][n_qo_heads] fp32 (nullable: not written)
+ *   scale : multiplies q . k before the softmax (1/sqrt(head_dim) for the
+ *           textbook form)
+ *
+ * One CTA per (sequence, KV head, split) streams that split's K/V pages through
+ * the block table into a shared-memory ring. The query heads of the KV head's
+ * GQA group are held in registers. Each CTA keeps a running max and sum (online
+ * softmax) and writes a partial (O, LSE) state. A merge kernel then combines the
+ * partials by log-sum-exp. Sequences whose pages fit in one split are written
+ * directly. The workspace (device, >= attn_decode_workspace_size bytes, 256-byte
+ * aligned) holds the partials; its contents on entry do not matter.
+ */
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* block_table, const int32_t* kv_lens, void* out, float* lse,
+                      int batch, int max_blocks_per_seq, int num_pages, int n_qo_heads,
+                      int n_kv_heads, int head_dim, int page_size, float scale, int num_splits,
+                      int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                      void* stream);
+
+/*
+ * Decode with FlashDecoding++'s asynchronised softmax with a unified maximum
+ * value ("【FlashAttention-V4，非官方】FlashDecoding++", sections 1 and 3).
+ * Scaled logits are exponentiated against the preset value `phi` (natural-log
+ * units, same units as lse), not against a running maximum. There is no per-tile
+ * max synchronisation, and partial states that share phi add up without
+ * rescaling. The pages leave the bound and the fallback open. This library's
+ * reading:
+ *   - when a tile holds a logit above phi + 60, the CTA raises its reference
+ *     value to that tile's max and rescales what it has accumulated;
+ *   - when a tile lies wholly below phi - 60 before anything was accumulated,
+ *     the reference value drops to the tile's max.
+ * Either event adds 1 to *fallback_count (nullable, int32 device counter,
+ * caller-cleared). The result equals attn_decode_paged up to rounding. Arguments,
+ * workspace and errors are as for attn_decode_paged.
+ */
+int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* kv_lens, void* out,
+                                  float* lse, int batch, int max_blocks_per_seq, int num_pages,
+                                  int n_qo_heads, int n_kv_heads, int head_dim, int page_size,
+                                  float scale, int num_splits, int dtype, float phi,
+                                  int32_t* fallback_count, void* workspace,
+                                  size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
+ * Merge two partial softmax states over disjoint key sets into one
+ * ("【FlashAttention-V4，非官方】FlashDecoding++", section 1: partial softmax
+ * results are updated at the end):
+ *   M = max(lse_a, lse_b), w_x = exp(lse_x - M),
+ *   out = (w_a out_a + w_b out_b) / (w_a + w_b), lse = M + ln(w_a + w_b).
+ * Two -inf sides give out = 0, lse = -inf.
+ *
+ *   out_a, out_b : fp32 [n_rows][head_dim];  lse_a, lse_b : fp32 [n_rows]
+ *   out          : out_dtype [n_rows][head_dim]; with out_dtype PKV_F32 it may
+ *                  alias out_a or out_b exactly
+ *   lse          : fp32 [n_rows] (nullable); may alias lse_a or lse_b exactly
+ * n_rows is every leading dimension flattened (e.g. batch * heads).
+ */
+int attn_merge_states(const float* out_a, const float* lse_a, const float* out_b,
+                      const float* lse_b, void* out, float* lse, int n_rows, int head_dim,
+                      int out_dtype, void* stream);
+
+/*
+ * Causal self-attention for prefill: query i of a sequence attends to keys
+ * 0..i of the same sequence. The query length equals the key length.
+ *
+ *   q, out : [batch][seq_len][n_qo_heads][head_dim], dtype, contiguous
+ *   k, v   : [batch][seq_len][n_kv_heads][head_dim], dtype, contiguous
+ *   lse    : fp32 [batch][n_qo_heads][seq_len] (nullable)
+ *
+ * The work is tiled as in FlashAttention: per tile, compute the scores,
+ * update the softmax statistics and accumulate the output on chip, so the
+ * T x T score matrix never reaches HBM ("快速注意力内核与算子融合", Q&A on
+ * FlashAttention). Both products run on the tcgen05 tensor cores with fp32
+ * accumulators in tensor memory, fed by TMA. All pointers must be 16-byte
+ * aligned.
+ */
+int attn_prefill_causal(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int batch, int seq_len, int n_qo_heads, int n_kv_heads, int head_dim,
+                        float scale, int dtype, int32_t* err_flag, void* stream);
+
+/* Workspace bytes attn_decode_cascade needs (fp32 partial states). (size_t)-1 on bad args. */
+size_t attn_cascade_workspace_size(int n_requests, int prefix_len, int max_suffix_blocks,
+                                   int n_qo_heads, int n_kv_heads, int head_dim, int page_size);
+
+/*
+ * Cascade (shared-prefix) decode. Every request's sequence is one shared prefix,
+ * whose pages are listed once in prefix_block_table, followed by that request's
+ * own suffix pages. Two readings meet here: "级联推理", which splits attention
+ * into stages that each handle part of the data (FlashInfer page, sections 2
+ * and 4), and prefix sharing in the paged cache ("快速注意力内核与算子融合", Q&A
+ * on paged attention). The prefix is attended once per KV head for the queries
+ * of all requests and that KV head's query heads, as one tensor-core product.
+ * The suffix is attended per request. The two partial states are merged by
+ * log-sum-exp.
+ *
+ *   q, out             : [n_requests][n_qo_heads][head_dim], dtype
+ *   lse                : fp32 [n_requests][n_qo_heads] (nullable)
+ *   prefix_block_table : int32 [ceil(prefix_len / page_size)]
+ *   suffix_block_table : int32 [n_requests][max_suffix_blocks]
+ *   suffix_lens        : int32 [n_requests] (0 allowed)
+ *   workspace          : >= attn_cascade_workspace_size bytes, 256-byte aligned
+ * The result equals attn_decode_paged over the concatenated sequences, up to
+ * rounding.
+ */
+int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* prefix_block_table, int prefix_len,
+                        const int32_t* suffix_block_table, const int32_t* suffix_lens, void* out,
+                        float* lse, int n_requests, int max_suffix_blocks, int num_pages,
+                        int n_qo_heads, int n_kv_heads, int head_dim, int page_size, float scale,
+                        int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                        void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_ATTN_H */

@@ -1,0 +1,277 @@
+// C ABI: argument checks, split planning, workspace sizing and dispatch.
+// No call allocates, frees, copies to the host or synchronises.
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace pkv {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested) {
+  int S;
+  if (requested > 0) {
+    S = requested < max_blocks ? requested : max_blocks;
+  } else {
+    // Enough CTAs for several waves on every SM if each sequence were full length,
+    // but never splits shorter than 16 pages.
+    const long units = (long)batch * n_kv_heads;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 148;
+    const long target = 4L * sms;
+    long s = (target + units - 1) / units;
+    long max_s = max_blocks / 16;
+    if (max_s < 1) max_s = 1;
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    S = (int)s;
+  }
+  const int pps = (max_blocks + S - 1) / S;
+  return SplitPlan{(max_blocks + pps - 1) / pps, pps};
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static size_t decode_ws_bytes(int batch, int n_qo_heads, int head_dim, int S) {
+  if (S <= 1) return 0;
+  const size_t rows = (size_t)batch * n_qo_heads;
+  return align_up(rows * S * head_dim * sizeof(float), 256) + align_up(rows * S * sizeof(float), 256);
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DecodeCall {
+  const void *q, *k_pages, *v_pages;
+  const int32_t *block_table, *kv_lens;
+  void* out;
+  float* lse;
+  int batch, max_blocks, num_pages, n_qo_heads, n_kv_heads, head_dim, page_size;
+  float scale;
+  int num_splits, dtype;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* err_flag;
+  cudaStream_t stream;
+};
+
+static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* fallback_count) {
+  if (c.batch < 0 || c.max_blocks < 1 || c.num_pages < 1 || c.n_qo_heads < 1 ||
+      c.n_kv_heads < 1 || c.head_dim < 1 || c.page_size < 1 || c.num_splits < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (c.n_qo_heads % c.n_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(c.scale) || (unified && !std::isfinite(phi))) return PKV_ERR_INVALID_ARG;
+  if (c.dtype != PKV_F32 && c.dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if ((long)c.max_blocks * c.page_size > 0x7fffffffL) return PKV_ERR_INVALID_ARG;
+  if (c.batch == 0) return PKV_OK;
+  if (!c.q || !c.k_pages || !c.v_pages || !c.block_table || !c.kv_lens || !c.out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(c.k_pages) || !aligned16(c.v_pages)) return PKV_ERR_INVALID_ARG;
+  const int G = c.n_qo_heads / c.n_kv_heads;
+  if (!decode_supported(c.dtype, c.head_dim, c.page_size, G)) return PKV_ERR_UNSUPPORTED;
+  if (c.batch > 65535 || c.n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, c.n_kv_heads, c.num_splits);
+  const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.head_dim, plan.num_splits);
+  if (need > 0 && (!c.workspace || c.workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(c.workspace) & 255u) != 0))
+    return PKV_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_DEVICE;
+
+  DecodeArgs a{};
+  a.q = c.q;
+  a.k_pages = c.k_pages;
+  a.v_pages = c.v_pages;
+  a.block_table = c.block_table;
+  a.kv_lens = c.kv_lens;
+  a.out = c.out;
+  a.lse = c.lse;
+  const size_t rows = (size_t)c.batch * c.n_qo_heads;
+  if (need > 0) {
+    a.part_o = static_cast<float*>(c.workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(c.workspace) +
+                                          align_up(rows * plan.num_splits * c.head_dim * sizeof(float), 256));
+  }
+  a.err_flag = c.err_flag;
+  a.batch = c.batch;
+  a.max_blocks = c.max_blocks;
+  a.num_pages = c.num_pages;
+  a.n_qo_heads = c.n_qo_heads;
+  a.n_kv_heads = c.n_kv_heads;
+  a.head_dim = c.head_dim;
+  a.page_size = c.page_size;
+  a.num_splits = plan.num_splits;
+  a.pages_per_split = plan.pages_per_split;
+  a.scale = c.scale;
+  a.dtype = c.dtype;
+  a.unified = unified;
+  a.phi = phi;
+  a.fallback_count = fallback_count;
+  return launch_decode(a, c.stream);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PKV_ERR_LAUNCH: return "CUDA launch failed";
+    case PKV_ERR_DEVICE: return "no usable CUDA device";
+    default: return "unknown status";
+  }
+}
+
+int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, int n_kv_heads,
+                           int head_dim, int page_size, int num_splits) {
+  if (batch < 0 || max_blocks_per_seq < 1 || n_qo_heads < 1 || n_kv_heads < 1 ||
+      head_dim < 1 || page_size < 1 || num_splits < 0 || n_qo_heads % n_kv_heads)
+    return PKV_ERR_INVALID_ARG;
+  return plan_decode_splits(batch, max_blocks_per_seq, n_kv_heads, num_splits).num_splits;
+}
+
+size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_heads,
+                                  int n_kv_heads, int head_dim, int page_size, int num_splits) {
+  const int S = attn_decode_num_splits(batch, max_blocks_per_seq, n_qo_heads, n_kv_heads,
+                                       head_dim, page_size, num_splits);
+  if (S < 0) return (size_t)-1;
+  return decode_ws_bytes(batch, n_qo_heads, head_dim, S);
+}
+
+int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                      const int32_t* block_table, const int32_t* kv_lens, void* out, float* lse,
+                      int batch, int max_blocks_per_seq, int num_pages, int n_qo_heads,
+                      int n_kv_heads, int head_dim, int page_size, float scale, int num_splits,
+                      int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                      void* stream) {
+  DecodeCall c{q, k_pages, v_pages, block_table, kv_lens, out, lse, batch, max_blocks_per_seq,
+               num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, dtype,
+               workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream)};
+  return decode_common(c, false, 0.0f, nullptr);
+}
+
+int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* kv_lens, void* out,
+                                  float* lse, int batch, int max_blocks_per_seq, int num_pages,
+                                  int n_qo_heads, int n_kv_heads, int head_dim, int page_size,
+                                  float scale, int num_splits, int dtype, float phi,
+                                  int32_t* fallback_count, void* workspace,
+                                  size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  DecodeCall c{q, k_pages, v_pages, block_table, kv_lens, out, lse, batch, max_blocks_per_seq,
+               num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, dtype,
+               workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream)};
+  return decode_common(c, true, phi, fallback_count);
+}
+
+int attn_merge_states(const float* out_a, const float* lse_a, const float* out_b,
+                      const float* lse_b, void* out, float* lse, int n_rows, int head_dim,
+                      int out_dtype, void* stream) {
+  if (n_rows < 0 || head_dim < 1) return PKV_ERR_INVALID_ARG;
+  if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (n_rows == 0) return PKV_OK;
+  if (!out_a || !lse_a || !out_b || !lse_b || !out) return PKV_ERR_INVALID_ARG;
+  if (n_rows > 65535L * 4 * 1024) return PKV_ERR_UNSUPPORTED;
+  return launch_merge_pair(out_a, lse_a, out_b, lse_b, out, lse, n_rows, head_dim, out_dtype,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int attn_prefill_causal(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int batch, int seq_len, int n_qo_heads, int n_kv_heads, int head_dim,
+                        float scale, int dtype, int32_t* err_flag, void* stream) {
+  if (batch < 0 || seq_len < 0 || n_qo_heads < 1 || n_kv_heads < 1 || head_dim < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (n_qo_heads % n_kv_heads || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (batch == 0 || seq_len == 0) return PKV_OK;
+  if (!q || !k || !v || !out) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_BF16 || head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  PrefillArgs a{q, k, v, out, lse, err_flag, batch, seq_len, n_qo_heads, n_kv_heads, head_dim, scale};
+  return launch_prefill(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_cascade_workspace_size(int n_requests, int prefix_len, int max_suffix_blocks,
+                                   int n_qo_heads, int n_kv_heads, int head_dim, int page_size) {
+  if (n_requests < 0 || prefix_len < 0 || max_suffix_blocks < 1 || n_qo_heads < 1 ||
+      n_kv_heads < 1 || head_dim < 1 || page_size < 1 || n_qo_heads % n_kv_heads)
+    return (size_t)-1;
+  const size_t rows = (size_t)n_requests * n_qo_heads;
+  const int chunks = cascade_prefix_chunks(prefix_len, n_requests, n_qo_heads, n_kv_heads);
+  return align_up((size_t)chunks * rows * head_dim * 4, 256) + align_up((size_t)chunks * rows * 4, 256) +
+         align_up(rows * head_dim * 4, 256) + align_up(rows * 4, 256);
+}
+
+int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* prefix_block_table, int prefix_len,
+                        const int32_t* suffix_block_table, const int32_t* suffix_lens, void* out,
+                        float* lse, int n_requests, int max_suffix_blocks, int num_pages,
+                        int n_qo_heads, int n_kv_heads, int head_dim, int page_size, float scale,
+                        int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                        void* stream) {
+  if (n_requests < 0 || prefix_len < 0 || max_suffix_blocks < 1 || num_pages < 1 ||
+      n_qo_heads < 1 || n_kv_heads < 1 || head_dim < 1 || page_size < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (n_qo_heads % n_kv_heads || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (n_requests == 0) return PKV_OK;
+  if (!q || !k_pages || !v_pages || !suffix_block_table || !suffix_lens || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (prefix_len > 0 && !prefix_block_table) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages)) return PKV_ERR_INVALID_ARG;
+  if (prefix_len % page_size) return PKV_ERR_UNSUPPORTED;
+  if (dtype != PKV_BF16 || head_dim != 128 || page_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (!decode_supported(dtype, head_dim, page_size, n_qo_heads / n_kv_heads))
+    return PKV_ERR_UNSUPPORTED;
+  const size_t need = attn_cascade_workspace_size(n_requests, prefix_len, max_suffix_blocks,
+                                                  n_qo_heads, n_kv_heads, head_dim, page_size);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_WORKSPACE;
+  CascadeArgs a{};
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.prefix_table = prefix_block_table;
+  a.prefix_len = prefix_len;
+  a.suffix_table = suffix_block_table;
+  a.suffix_lens = suffix_lens;
+  a.out = out;
+  a.lse = lse;
+  a.n_requests = n_requests;
+  a.max_suffix_blocks = max_suffix_blocks;
+  a.num_pages = num_pages;
+  a.n_qo_heads = n_qo_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = head_dim;
+  a.page_size = page_size;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.err_flag = err_flag;
+  const size_t rows = (size_t)n_requests * n_qo_heads;
+  a.prefix_chunks = cascade_prefix_chunks(prefix_len, n_requests, n_qo_heads, n_kv_heads);
+  char* w = static_cast<char*>(workspace);
+  a.pre_o = reinterpret_cast<float*>(w);
+  w += align_up((size_t)a.prefix_chunks * rows * head_dim * 4, 256);
+  a.pre_lse = reinterpret_cast<float*>(w);
+  w += align_up((size_t)a.prefix_chunks * rows * 4, 256);
+  a.suf_o = reinterpret_cast<float*>(w);
+  w += align_up(rows * head_dim * 4, 256);
+  a.suf_lse = reinterpret_cast<float*>(w);
+  return launch_cascade(a, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

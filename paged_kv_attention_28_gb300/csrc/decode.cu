@@ -1,0 +1,127 @@
+// Online-softmax paged decode, the split merge, and the pairwise state merge.
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+// Combines the live splits of each (sequence, query head) row by log-sum-exp:
+// M = max_s lse_s, w_s = exp(lse_s - M), out = sum w_s O_s / sum w_s,
+// lse = M + ln sum w_s. FlashDecoding computes the partials independently and
+// updates them all at the end ("【FlashAttention-V4，非官方】FlashDecoding++",
+// section 1). Rows whose sequence fits in one split were written by the
+// decode kernel and are skipped here. One warp per row.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) merge_splits_kernel(const DecodeArgs a) {
+  constexpr int DL = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= a.batch * a.n_qo_heads) return;
+  const int b = row / a.n_qo_heads;
+  const int P = a.page_size;
+  const int L = __ldg(a.kv_lens + b);
+  if (L < 0 || L > a.max_blocks * P) return;  // the decode kernel wrote NaN
+  const int nblk = (L + P - 1) / P;
+  const int n_live = (nblk + a.pages_per_split - 1) / a.pages_per_split;
+  if (n_live < 2) return;
+  const float* pl = a.part_lse + (size_t)row * a.num_splits;
+  const float* po = a.part_o + (size_t)row * a.num_splits * D;
+  float M = -INFINITY;
+  for (int s = lane; s < n_live; s += 32) M = fmaxf(M, pl[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float acc[DL];
+#pragma unroll
+  for (int e = 0; e < DL; ++e) acc[e] = 0.0f;
+  float Lsum = 0.0f;
+  for (int s = 0; s < n_live; ++s) {
+    const float w = ex2((pl[s] - M) * kLog2e);
+    Lsum += w;
+    float o[DL];
+    if constexpr (DL == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(po + (size_t)s * D + lane * 4);
+      o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(po + (size_t)s * D + lane * 2);
+      o[0] = x.x; o[1] = x.y;
+    }
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, o[e], acc[e]);
+  }
+  const float inv = 1.0f / Lsum;
+  T* out = static_cast<T*>(a.out) + (size_t)row * D + lane * DL;
+#pragma unroll
+  for (int e = 0; e < DL; ++e) out[e] = from_f32<T>(acc[e] * inv);
+  if (a.lse && lane == 0) a.lse[row] = M + logf(Lsum);
+}
+
+template <typename T, int D>
+int launch_merge_t(const DecodeArgs& a, cudaStream_t stream) {
+  const int rows = a.batch * a.n_qo_heads;
+  merge_splits_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+int launch_merge_splits(const DecodeArgs& a, cudaStream_t stream) {
+  if (a.dtype == PKV_F32) {
+    if (a.head_dim == 64) return launch_merge_t<float, 64>(a, stream);
+    if (a.head_dim == 128) return launch_merge_t<float, 128>(a, stream);
+  } else {
+    if (a.head_dim == 64) return launch_merge_t<__nv_bfloat16, 64>(a, stream);
+    if (a.head_dim == 128) return launch_merge_t<__nv_bfloat16, 128>(a, stream);
+  }
+  return PKV_ERR_UNSUPPORTED;
+}
+
+int dispatch_decode_unified(const DecodeArgs& a, cudaStream_t stream);  // decode_um.cu
+
+bool decode_supported(int dtype, int head_dim, int page_size, int group) {
+  return (dtype == PKV_F32 || dtype == PKV_BF16) && (head_dim == 64 || head_dim == 128) &&
+         page_size == 16 && (group == 1 || group == 2 || group == 4 || group == 8);
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  const int rc = a.unified ? dispatch_decode_unified(a, stream) : dispatch_decode<false>(a, stream);
+  if (rc != PKV_OK) return rc;
+  if (a.num_splits > 1) return launch_merge_splits(a, stream);
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------------ pairwise merge
+
+template <typename T>
+__global__ void __launch_bounds__(128)
+merge_pair_kernel(const float* oa, const float* la, const float* ob,
+                  const float* lb, T* out, float* lse, int n_rows, int D) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  const float a = la[row];
+  const float bb = lb[row];
+  __syncwarp();  // every lane has read lse before lane 0 may overwrite it in place
+  const float M = fmaxf(a, bb);
+  const bool empty = (M == -INFINITY);
+  const float wa = empty ? 0.0f : ex2((a - M) * kLog2e);
+  const float wb = empty ? 0.0f : ex2((bb - M) * kLog2e);
+  const float inv = empty ? 0.0f : 1.0f / (wa + wb);
+  for (int d = lane; d < D; d += 32) {
+    const size_t i = (size_t)row * D + d;
+    const float x = empty ? 0.0f : (wa * oa[i] + wb * ob[i]) * inv;
+    out[i] = from_f32<T>(x);
+  }
+  if (lse && lane == 0) lse[row] = empty ? -INFINITY : M + logf(wa + wb);
+}
+
+int launch_merge_pair(const float* out_a, const float* lse_a, const float* out_b,
+                      const float* lse_b, void* out, float* lse, int n_rows, int head_dim,
+                      int out_dtype, cudaStream_t stream) {
+  if (n_rows == 0) return PKV_OK;
+  const int grid = (n_rows + 3) / 4;
+  if (out_dtype == PKV_F32)
+    merge_pair_kernel<float><<<grid, 128, 0, stream>>>(out_a, lse_a, out_b, lse_b,
+                                                      static_cast<float*>(out), lse, n_rows, head_dim);
+  else
+    merge_pair_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(
+        out_a, lse_a, out_b, lse_b, static_cast<__nv_bfloat16*>(out), lse, n_rows, head_dim);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+}  // namespace pkv

@@ -1,0 +1,519 @@
+// Paged single-token decode kernel (sm_103a).
+//
+// One CTA per (KV split, KV head, sequence). A producer warp streams the
+// split's (page, KV head) tiles of K and V (page_size x head_dim contiguous
+// elements each) through the block table into a ring of shared-memory stages.
+// It uses one-dimensional bulk TMA copies that complete on an mbarrier.
+// Consumer warps take the pages in turn. Each keeps the query heads of its GQA
+// group in registers and reduces the q.k dot products and the running
+// max/sum with __shfl_xor_sync. The block-table mapping is from
+// "快速注意力内核与算子融合" (Q&A on paged attention); the warp-shuffle
+// reductions are the warp-level primitives of the FlashInfer page (section 3).
+//
+// Softmax statistics are carried in base-2 units: logits are prescaled by
+// scale*log2(e), exponentials are ex2, and lse = (ref + log2 l) * ln 2.
+//
+// Two ways to pick the reference value that logits are exponentiated against:
+//  * online (FlashAttention/FlashDecoding): the running max. When a chunk
+//    raises it, the accumulated sum and output are rescaled.
+//  * unified (FlashDecoding++ asynchronised softmax, "【FlashAttention-V4，
+//    非官方】FlashDecoding++" sections 1 and 3): a preset phi shared by every
+//    partial, with no max tracking. A warp moves off phi only when a chunk
+//    would overflow (a logit above phi + beta) or, for its first chunk, would
+//    underflow entirely (every logit below phi - beta). Each such event is
+//    counted.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Unified-max safety margin in natural-log units: exp(60) * 2^20 terms stays
+// far below FLT_MAX, and a chunk 60 below the reference contributes < e^-60.
+constexpr float kUnifiedBeta = 60.0f;
+
+template <typename T, int D, int P, int G>
+struct DecodeCfg {
+  static constexpr int ES = sizeof(T);
+  static constexpr int LPT = (G >= 8) ? 16 : 8;   // lanes that share one token row
+  static constexpr int TPI = 32 / LPT;             // token rows a warp covers per step
+  static constexpr int DPL = D / LPT;              // head dims held per lane
+  static constexpr int VEC = (16 / ES < DPL) ? 16 / ES : DPL;  // elements per smem load
+  static constexpr int NV = DPL / VEC;             // loads per row per lane
+  static constexpr int ITERS = P / TPI;            // steps per page
+  static constexpr int NIT_MAX = (32 / G) > 0 ? (32 / G) : 1;
+  static constexpr int NIT = ITERS < NIT_MAX ? ITERS : NIT_MAX;  // steps per softmax chunk
+  static constexpr int NCHUNK = ITERS / NIT;
+  static constexpr int TILE = P * D * ES;          // bytes of one (page, KV head) tile
+  static constexpr int NW = 4;                     // consumer warps
+  static constexpr int NSTAGE = 8;                 // ring depth (multiple of NW)
+  static constexpr int THREADS = (NW + 1) * 32;
+  static constexpr int MIN_BLOCKS = (G >= 4) ? 2 : 3;
+  static constexpr int BAR_OFF = 2 * NSTAGE * TILE;
+  static constexpr int FLAG_OFF = BAR_OFF + 2 * NSTAGE * 8;
+  static constexpr int SMEM = FLAG_OFF + 16;
+  static_assert(D % LPT == 0 && DPL % VEC == 0, "head_dim split");
+  static_assert(P % TPI == 0 && ITERS % NIT == 0, "page split");
+  static_assert(NSTAGE % NW == 0, "stage ownership");
+  static_assert(TILE % 16 == 0, "bulk copy granularity");
+  static_assert(NW * G * (D + 2) * 4 <= 2 * NSTAGE * TILE, "combine scratch fits in the ring");
+};
+
+struct DecodeFlags {
+  int abort_;
+  int bad_page;
+  int issued;
+  int fallbacks;
+};
+
+template <typename T, int VEC>
+__device__ __forceinline__ void load_row_vec(const T* p, float* f) {
+  if constexpr (sizeof(T) == 4) {
+    static_assert(VEC == 4 || VEC == 2, "fp32 vector");
+    if constexpr (VEC == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p);
+      f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(p);
+      f[0] = x.x; f[1] = x.y;
+    }
+  } else {
+    static_assert(VEC == 8 || VEC == 4, "bf16 vector");
+    // bf16 -> fp32 is a 16-bit left shift of the bit pattern.
+    if constexpr (VEC == 8) {
+      const uint4 x = *reinterpret_cast<const uint4*>(p);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2*>(p);
+      f[0] = __uint_as_float(x.x << 16);
+      f[1] = __uint_as_float(x.x & 0xffff0000u);
+      f[2] = __uint_as_float(x.y << 16);
+      f[3] = __uint_as_float(x.y & 0xffff0000u);
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Writes the rows of one (sequence, KV head) group: NaN (bad input), or 0 / -inf
+// (empty sequence). Used by the split-0 CTA only.
+template <typename T, int D, int G>
+__device__ void write_group_const(const DecodeArgs& a, int b, int g, float o, float l) {
+  T* out = static_cast<T*>(a.out);
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int h = g * G + idx / D;
+    out[((size_t)b * a.n_qo_heads + h) * D + idx % D] = from_f32<T>(o);
+    if (a.lse && idx % D == 0) a.lse[(size_t)b * a.n_qo_heads + h] = l;
+  }
+}
+
+template <typename T, int D, int P, int G, bool UNIFIED>
+__global__ void __launch_bounds__(DecodeCfg<T, D, P, G>::THREADS, DecodeCfg<T, D, P, G>::MIN_BLOCKS)
+decode_paged_kernel(const DecodeArgs a) {
+  using C = DecodeCfg<T, D, P, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int split = blockIdx.x;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+
+  const int kv_len = __ldg(a.kv_lens + b);
+  if (kv_len < 0 || kv_len > a.max_blocks * P) {
+    if (split == 0) {
+      if (threadIdx.x == 0) set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
+      write_group_const<T, D, G>(a, b, g, NAN, NAN);
+    }
+    return;
+  }
+  const int nblk = (kv_len + P - 1) / P;
+  const int n_live = (nblk + a.pages_per_split - 1) / a.pages_per_split;
+  if (n_live == 0) {
+    if (split == 0) write_group_const<T, D, G>(a, b, g, 0.0f, -INFINITY);
+    return;
+  }
+  if (split >= n_live) return;
+  const int first = split * a.pages_per_split;
+  const int n_pages = min(a.pages_per_split, nblk - first);
+  const bool final_write = (n_live == 1);
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + C::BAR_OFF;
+  const uint32_t bar_empty = bar_full + C::NSTAGE * 8;
+  DecodeFlags* flags = reinterpret_cast<DecodeFlags*>(smem + C::FLAG_OFF);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    flags->abort_ = 0;
+    flags->bad_page = 0;
+    flags->issued = 0;
+    flags->fallbacks = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == C::NW) {
+    // ------------------------------------------------------------ producer warp
+    const int32_t* trow = a.block_table + (size_t)b * a.max_blocks + first;
+    const uint64_t pol = policy_evict_first();
+    const char* kbase = static_cast<const char*>(a.k_pages);
+    const char* vbase = static_cast<const char*>(a.v_pages);
+    bool ok = true;
+    int issued = 0;
+    for (int base = 0; base < n_pages && ok; base += 32) {
+      const int idx = base + lane;
+      const int phys = (idx < n_pages) ? __ldg(trow + idx) : 0;
+      const bool bad = (idx < n_pages) && (phys < 0 || phys >= a.num_pages);
+      const unsigned badm = __ballot_sync(0xffffffffu, bad);
+      if (badm && lane == 0) {
+        set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
+        flags->bad_page = 1;
+      }
+      const int cnt = min(32, n_pages - base);
+      for (int k = 0; k < cnt; ++k) {
+        const int p = __shfl_sync(0xffffffffu, phys, k);
+        const int i = base + k;
+        const int s = i % C::NSTAGE;
+        const int use = i / C::NSTAGE;
+        if (lane == 0) {
+          if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+            ok = false;
+          } else if ((badm >> k) & 1u) {
+            mbar_arrive(bar_full + 8 * s);  // completes the phase with no data
+            issued = i + 1;
+          } else {
+            const size_t off = ((size_t)p * a.n_kv_heads + g) * C::TILE;
+            mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::TILE);
+            bulk_g2s_hint(sbase + s * C::TILE, kbase + off, C::TILE, bar_full + 8 * s, pol);
+            bulk_g2s_hint(sbase + (C::NSTAGE + s) * C::TILE, vbase + off, C::TILE,
+                          bar_full + 8 * s, pol);
+            issued = i + 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+    }
+    if (lane == 0) {
+      flags->issued = issued;
+      if (!ok) {
+        flags->abort_ = 1;
+        set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- consumer warps
+  const int tg = lane / C::LPT;  // token row within a step
+  const int j = lane % C::LPT;   // column group within the row
+  float ref[G], lsum[G], acc[G][C::DPL];
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) {
+    ref[gi] = UNIFIED ? a.phi * kLog2e : -INFINITY;
+    lsum[gi] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < C::DPL; ++e) acc[gi][e] = 0.0f;
+  }
+  int fallbacks = 0;
+
+  if (warp < C::NW) {
+    float qr[G][C::DPL];
+    const float qscale = a.scale * kLog2e;
+    const T* qp = static_cast<const T*>(a.q) + ((size_t)b * a.n_qo_heads + g * G) * D;
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+      for (int c = 0; c < C::NV; ++c)
+#pragma unroll
+        for (int e = 0; e < C::VEC; ++e)
+          qr[gi][c * C::VEC + e] = to_f32<T>(qp[gi * D + c * C::LPT * C::VEC + j * C::VEC + e]) * qscale;
+
+    const float beta2 = kUnifiedBeta * kLog2e;
+    bool first_chunk = true;
+    for (int i = warp; i < n_pages; i += C::NW) {
+      const int s = i % C::NSTAGE;
+      if (!mbar_wait(bar_full + 8 * s, (i / C::NSTAGE) & 1)) {
+        if (lane == 0) {
+          flags->abort_ = 1;
+          set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+        }
+        break;
+      }
+      const T* kt = reinterpret_cast<const T*>(smem + s * C::TILE);
+      const T* vt = reinterpret_cast<const T*>(smem + (C::NSTAGE + s) * C::TILE);
+      const int valid = min(P, kv_len - (first + i) * P);
+#pragma unroll
+      for (int ch = 0; ch < C::NCHUNK; ++ch) {
+        float sc[C::NIT][G];
+#pragma unroll
+        for (int it = 0; it < C::NIT; ++it) {
+          const int t = (ch * C::NIT + it) * C::TPI + tg;
+          float kf[C::DPL];
+#pragma unroll
+          for (int c = 0; c < C::NV; ++c)
+            load_row_vec<T, C::VEC>(kt + t * D + c * C::LPT * C::VEC + j * C::VEC, kf + c * C::VEC);
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            float d0 = 0.0f, d1 = 0.0f;
+#pragma unroll
+            for (int e = 0; e < C::DPL; e += 2) {
+              d0 = fmaf(qr[gi][e], kf[e], d0);
+              d1 = fmaf(qr[gi][e + 1], kf[e + 1], d1);
+            }
+            sc[it][gi] = d0 + d1;
+          }
+        }
+#pragma unroll
+        for (int off = 1; off < C::LPT; off <<= 1)
+#pragma unroll
+          for (int it = 0; it < C::NIT; ++it)
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) sc[it][gi] += __shfl_xor_sync(0xffffffffu, sc[it][gi], off);
+#pragma unroll
+        for (int it = 0; it < C::NIT; ++it) {
+          const int t = (ch * C::NIT + it) * C::TPI + tg;
+          if (t >= valid) {
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) sc[it][gi] = -INFINITY;
+          }
+        }
+
+        if constexpr (!UNIFIED) {
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            float mx = sc[0][gi];
+#pragma unroll
+            for (int it = 1; it < C::NIT; ++it) mx = fmaxf(mx, sc[it][gi]);
+#pragma unroll
+            for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            if (mx > ref[gi]) {  // warp-uniform: every lane holds the same mx and ref
+              const float alpha = ex2(ref[gi] - mx);
+              ref[gi] = mx;
+              lsum[gi] *= alpha;
+#pragma unroll
+              for (int e = 0; e < C::DPL; ++e) acc[gi][e] *= alpha;
+            }
+          }
+        } else {
+          bool viol = false;
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            bool all_low = true;
+#pragma unroll
+            for (int it = 0; it < C::NIT; ++it) {
+              viol |= sc[it][gi] > ref[gi] + beta2;
+              all_low &= sc[it][gi] < ref[gi] - beta2;
+            }
+            if (first_chunk) viol |= __all_sync(0xffffffffu, all_low);
+          }
+          if (__any_sync(0xffffffffu, viol)) {
+            // Fallback: move each head's reference to this chunk's max where needed.
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              float mx = sc[0][gi];
+#pragma unroll
+              for (int it = 1; it < C::NIT; ++it) mx = fmaxf(mx, sc[it][gi]);
+#pragma unroll
+              for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+              const bool hi = mx > ref[gi] + beta2;
+              const bool lo = first_chunk && mx < ref[gi] - beta2;
+              if (hi || lo) {
+                const float alpha = ex2(ref[gi] - mx);
+                ref[gi] = mx;
+                lsum[gi] *= alpha;
+#pragma unroll
+                for (int e = 0; e < C::DPL; ++e) acc[gi][e] *= alpha;
+                ++fallbacks;
+              }
+            }
+          }
+          first_chunk = false;
+        }
+
+#pragma unroll
+        for (int it = 0; it < C::NIT; ++it)
+#pragma unroll
+          for (int gi = 0; gi < G; ++gi) {
+            sc[it][gi] = ex2(sc[it][gi] - ref[gi]);
+            lsum[gi] += sc[it][gi];
+          }
+#pragma unroll
+        for (int it = 0; it < C::NIT; ++it) {
+          const int t = (ch * C::NIT + it) * C::TPI + tg;
+          float vf[C::DPL];
+#pragma unroll
+          for (int c = 0; c < C::NV; ++c)
+            load_row_vec<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, vf + c * C::VEC);
+          if (t < valid) {
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+              for (int e = 0; e < C::DPL; ++e) acc[gi][e] = fmaf(sc[it][gi], vf[e], acc[gi][e]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    }
+
+    // Sum the per-row partials over the token rows of the warp (lanes with equal j).
+#pragma unroll
+    for (int off = C::LPT; off < 32; off <<= 1)
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        lsum[gi] += __shfl_xor_sync(0xffffffffu, lsum[gi], off);
+#pragma unroll
+        for (int e = 0; e < C::DPL; ++e) acc[gi][e] += __shfl_xor_sync(0xffffffffu, acc[gi][e], off);
+      }
+  }
+
+  __syncthreads();
+  if (flags->abort_) {
+    // Wait (bounded) for every copy that was issued, then mark the rows as failed.
+    if (threadIdx.x == 0) {
+      const int issued = flags->issued;
+      for (int s = 0; s < C::NSTAGE && s < issued; ++s) {
+        const int last_use = (issued - 1 - s) / C::NSTAGE;
+        mbar_wait(bar_full + 8 * s, last_use & 1);
+      }
+    }
+    __syncthreads();
+    if (final_write) {
+      write_group_const<T, D, G>(a, b, g, NAN, NAN);
+    } else {
+      for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const size_t row = (size_t)b * a.n_qo_heads + g * G + idx / D;
+        a.part_o[(row * a.num_splits + split) * D + idx % D] = NAN;
+        if (idx % D == 0) a.part_lse[row * a.num_splits + split] = NAN;
+      }
+    }
+    return;
+  }
+
+  // Every issued copy has landed and been consumed: the ring is free for the combine.
+  float* cref = reinterpret_cast<float*>(smem);
+  float* cl = cref + C::NW * G;
+  float* cacc = cl + C::NW * G;
+  if (warp < C::NW) {
+    if (lane == 0) {
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        cref[warp * G + gi] = ref[gi];
+        cl[warp * G + gi] = lsum[gi];
+      }
+      if constexpr (UNIFIED) {
+        if (fallbacks) atomicAdd(&flags->fallbacks, fallbacks);
+      }
+    }
+    if (tg == 0) {
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+        for (int c = 0; c < C::NV; ++c)
+#pragma unroll
+          for (int e = 0; e < C::VEC; ++e)
+            cacc[(warp * G + gi) * D + c * C::LPT * C::VEC + j * C::VEC + e] = acc[gi][c * C::VEC + e];
+    }
+  }
+  __syncthreads();
+
+  const bool poisoned = flags->bad_page != 0;
+  if constexpr (UNIFIED) {
+    if (threadIdx.x == 0 && flags->fallbacks && a.fallback_count)
+      atomicAdd(a.fallback_count, flags->fallbacks);
+  }
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int gi = idx / D;
+    const int d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, cref[w * G + gi]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) {
+      const float f = ex2(cref[w * G + gi] - M);  // 0 for a warp that saw no page
+      L = fmaf(f, cl[w * G + gi], L);
+      O = fmaf(f, cacc[(w * G + gi) * D + d], O);
+    }
+    O = O / L;
+    float lse = (M + log2f(L)) * kLn2;
+    if (poisoned) {
+      O = NAN;
+      lse = NAN;
+    }
+    const int h = g * G + gi;
+    const size_t row = (size_t)b * a.n_qo_heads + h;
+    if (final_write) {
+      static_cast<T*>(a.out)[row * D + d] = from_f32<T>(O);
+      if (a.lse && d == 0) a.lse[row] = lse;
+    } else {
+      a.part_o[(row * a.num_splits + split) * D + d] = O;
+      if (d == 0) a.part_lse[row * a.num_splits + split] = lse;
+    }
+  }
+}
+
+template <typename T, int D, int P, int G, bool UNIFIED>
+int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
+  using C = DecodeCfg<T, D, P, G>;
+  auto kern = decode_paged_kernel<T, D, P, G, UNIFIED>;
+  static int configured_mask = 0;  // one bit per device ordinal < 32
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 32 && !(configured_mask & (1 << dev))) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return PKV_ERR_LAUNCH;
+    configured_mask |= (1 << dev);
+  }
+  dim3 grid(a.num_splits, a.n_kv_heads, a.batch);
+  kern<<<grid, C::THREADS, C::SMEM, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+template <bool UNIFIED>
+int dispatch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  const int G = a.n_qo_heads / a.n_kv_heads;
+#define PKV_DEC_CASE(TT, DD, GG)                                   \
+  if (a.head_dim == DD && G == GG)                                 \
+    return launch_decode_t<TT, DD, 16, GG, UNIFIED>(a, stream);
+#define PKV_DEC_DT(TT)                                             \
+  PKV_DEC_CASE(TT, 64, 1) PKV_DEC_CASE(TT, 64, 2) PKV_DEC_CASE(TT, 64, 4) PKV_DEC_CASE(TT, 64, 8) \
+  PKV_DEC_CASE(TT, 128, 1) PKV_DEC_CASE(TT, 128, 2) PKV_DEC_CASE(TT, 128, 4) PKV_DEC_CASE(TT, 128, 8)
+  if (a.page_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (a.dtype == PKV_F32) {
+    PKV_DEC_DT(float)
+  } else if (a.dtype == PKV_BF16) {
+    PKV_DEC_DT(__nv_bfloat16)
+  }
+#undef PKV_DEC_DT
+#undef PKV_DEC_CASE
+  return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

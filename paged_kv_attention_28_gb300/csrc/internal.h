@@ -1,0 +1,86 @@
+// Host-side declarations shared by the launch layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pkv_attn.h"
+
+namespace pkv {
+
+// Everything a decode launch needs (device pointers and resolved sizes).
+struct DecodeArgs {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* block_table;
+  const int32_t* kv_lens;
+  void* out;
+  float* lse;
+  float* part_o;    // [batch][n_qo_heads][num_splits][head_dim], used when num_splits > 1
+  float* part_lse;  // [batch][n_qo_heads][num_splits]
+  int32_t* err_flag;
+  int batch, max_blocks, num_pages, n_qo_heads, n_kv_heads, head_dim, page_size;
+  int num_splits, pages_per_split;
+  float scale;
+  int dtype;
+  // unified-max variant
+  bool unified;
+  float phi;
+  int32_t* fallback_count;
+};
+
+struct SplitPlan {
+  int num_splits;
+  int pages_per_split;
+};
+
+int device_sm_count();
+SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested);
+
+// Enqueues the decode kernel (and the merge kernel when num_splits > 1).
+int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+bool decode_supported(int dtype, int head_dim, int page_size, int group);
+
+int launch_merge_pair(const float* out_a, const float* lse_a, const float* out_b,
+                      const float* lse_b, void* out, float* lse, int n_rows, int head_dim,
+                      int out_dtype, cudaStream_t stream);
+
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int32_t* err_flag;
+  int batch, seq_len, n_qo_heads, n_kv_heads, head_dim;
+  float scale;
+};
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+struct CascadeArgs {
+  const void* q;
+  const void* k_pages;
+  const void* v_pages;
+  const int32_t* prefix_table;
+  int prefix_len;
+  const int32_t* suffix_table;
+  const int32_t* suffix_lens;
+  void* out;
+  float* lse;
+  int n_requests, max_suffix_blocks, num_pages, n_qo_heads, n_kv_heads, head_dim, page_size;
+  float scale;
+  int dtype;
+  int32_t* err_flag;
+  // workspace carve-up
+  float* pre_o;     // [prefix_chunks][n_requests][n_qo_heads][head_dim]
+  float* pre_lse;   // [prefix_chunks][n_requests][n_qo_heads]
+  float* suf_o;     // [n_requests][n_qo_heads][head_dim]
+  float* suf_lse;   // [n_requests][n_qo_heads]
+  int prefix_chunks;
+};
+int cascade_prefix_chunks(int prefix_len, int n_requests, int n_qo_heads, int n_kv_heads);
+int launch_cascade(const CascadeArgs& a, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,113 @@
+"""The C-ABI library loads on a machine without a GPU and exports what the header declares.
+
+No compute call is made here. Only host-side argument checking, split planning
+and workspace sizing run, and every call shown returns before any launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv_attn.h")
+
+
+@pytest.fixture(scope="module")
+def b():
+    from paged_kv_attention_28_gb300 import build
+    build.build(quiet=True)
+    from paged_kv_attention_28_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(b):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(b.lib, n), n
+    assert sorted(b.EXPORTS) == names
+
+
+def test_status_strings(b):
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(b.status_string(code), str) and b.status_string(code)
+
+
+def test_split_planning(b):
+    # explicit request: 2048 pages in 32 splits of 64 pages
+    assert b.decode_num_splits(4, 2048, 32, 8, 128, 16, 32) == 32
+    # a request above the page count is capped
+    assert b.decode_num_splits(1, 4, 8, 8, 64, 16, 100) == 4
+    # uneven: 10 pages in 3 splits -> 4 pages per split -> 3 splits
+    assert b.decode_num_splits(1, 10, 8, 8, 64, 16, 3) == 3
+    # 10 pages in 4 splits -> 3 pages per split -> 4 splits
+    assert b.decode_num_splits(1, 10, 8, 8, 64, 16, 4) == 4
+    # automatic choice: at least one split, never splits below 16 pages
+    s = b.decode_num_splits(16, 256, 32, 32, 128, 16, 0)
+    assert 1 <= s <= 16
+    assert b.decode_num_splits(1, 16, 8, 8, 64, 16, 0) == 1
+
+
+def test_workspace_size(b):
+    assert b.decode_workspace_size(1, 16, 8, 8, 64, 16, 1) == 0
+    n = b.decode_workspace_size(4, 2048, 32, 8, 128, 16, 32)
+    rows = 4 * 32
+    assert n == rows * 32 * 128 * 4 + ((rows * 32 * 4 + 255) // 256) * 256
+    with pytest.raises(b.AttnError):
+        b.decode_workspace_size(1, 0, 8, 8, 64, 16, 1)
+    with pytest.raises(b.AttnError):
+        b.decode_workspace_size(1, 16, 6, 4, 64, 16, 1)
+
+
+def test_invalid_arguments_rejected_before_launch(b):
+    L = b.lib
+    nul = None
+    # null pointers with a non-empty batch
+    assert L.attn_decode_paged(nul, nul, nul, nul, nul, nul, nul, 1, 1, 1, 8, 8, 64, 16, 1.0, 0,
+                               b.PKV_F32, nul, 0, nul, nul) == b.PKV_ERR_INVALID_ARG
+    # heads not a multiple
+    assert L.attn_decode_paged(nul, nul, nul, nul, nul, nul, nul, 1, 1, 1, 6, 4, 64, 16, 1.0, 0,
+                               b.PKV_F32, nul, 0, nul, nul) == b.PKV_ERR_INVALID_ARG
+    # bad dtype
+    assert L.attn_decode_paged(nul, nul, nul, nul, nul, nul, nul, 1, 1, 1, 8, 8, 64, 16, 1.0, 0,
+                               9, nul, 0, nul, nul) == b.PKV_ERR_INVALID_ARG
+    # non-finite scale
+    assert L.attn_decode_paged(nul, nul, nul, nul, nul, nul, nul, 1, 1, 1, 8, 8, 64, 16,
+                               float("nan"), 0, b.PKV_F32, nul, 0, nul, nul) == b.PKV_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    assert L.attn_decode_paged(nul, nul, nul, nul, nul, nul, nul, 0, 1, 1, 8, 8, 64, 16, 1.0, 0,
+                               b.PKV_F32, nul, 0, nul, nul) == b.PKV_OK
+    assert L.attn_merge_states(nul, nul, nul, nul, nul, nul, 0, 64, b.PKV_F32, nul) == b.PKV_OK
+    assert L.attn_merge_states(nul, nul, nul, nul, nul, nul, 3, 64, b.PKV_F32, nul) == b.PKV_ERR_INVALID_ARG
+    assert L.attn_prefill_causal(nul, nul, nul, nul, nul, 0, 16, 8, 8, 128, 1.0, b.PKV_BF16, nul,
+                                 nul) == b.PKV_OK
+    assert L.attn_prefill_causal(nul, nul, nul, nul, nul, 1, 16, 8, 8, 128, 1.0, b.PKV_BF16, nul,
+                                 nul) == b.PKV_ERR_INVALID_ARG
+
+
+def test_unsupported_shapes_are_reported(b):
+    # pointers that are aligned but never dereferenced: UNSUPPORTED is returned first
+    p = ctypes.c_void_p(1 << 20)
+    L = b.lib
+    assert L.attn_decode_paged(p, p, p, p, p, p, p, 1, 1, 1, 8, 8, 96, 16, 1.0, 1, b.PKV_F32,
+                               None, 0, None, None) == b.PKV_ERR_UNSUPPORTED
+    assert L.attn_decode_paged(p, p, p, p, p, p, p, 1, 1, 1, 8, 8, 64, 32, 1.0, 1, b.PKV_F32,
+                               None, 0, None, None) == b.PKV_ERR_UNSUPPORTED
+    assert L.attn_decode_paged(p, p, p, p, p, p, p, 1, 1, 1, 48, 3, 64, 16, 1.0, 1, b.PKV_F32,
+                               None, 0, None, None) == b.PKV_ERR_UNSUPPORTED
+    assert L.attn_prefill_causal(p, p, p, p, p, 1, 16, 8, 8, 64, 1.0, b.PKV_BF16, None,
+                                 None) == b.PKV_ERR_UNSUPPORTED
+    # workspace needed but missing
+    assert L.attn_decode_paged(p, p, p, p, p, p, p, 1, 64, 64, 8, 8, 64, 16, 1.0, 4, b.PKV_F32,
+                               None, 0, None, None) == b.PKV_ERR_WORKSPACE
+    # misaligned page pool
+    q = ctypes.c_void_p((1 << 20) + 4)
+    assert L.attn_decode_paged(p, q, p, p, p, p, p, 1, 1, 1, 8, 8, 64, 16, 1.0, 1, b.PKV_F32,
+                               None, 0, None, None) == b.PKV_ERR_INVALID_ARG
