@@ -72,23 +72,33 @@ def profiled_traffic(kernel_key, src_hash, units_now):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons around the timed region.
 
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    ``mark_start``/``mark_end`` bracket the timed region. The summary uses the
+    samples taken inside it, or the nearest sample on each side when the region
+    is shorter than the sampling period. ``settle`` keeps the GPU busy until a
+    sample exists on the needed side, so that the samples reflect clocks under load.
+    """
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.f = None
+        self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
-            self.f = tempfile.TemporaryFile(mode="w+")
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -101,27 +111,63 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.fh.close()
+
+    def _rows(self):
+        import datetime
+        rows = []
+        if self.path is None:
+            return rows
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(p[1]), float(p[2]), p[5:9]))
+                except ValueError:
+                    continue
+        return rows
+
+    def settle(self, busy, after=None, timeout=5.0):
+        """Run ``busy()`` until a sample exists (after time ``after`` when given)."""
+        if self.proc is None:
+            return
+        t_end = time.time() + timeout
+        while time.time() < t_end:
+            rows = self._rows()
+            if rows and (after is None or rows[-1][0] > after):
+                return
+            for _ in range(20):
+                busy()
+            torch.cuda.synchronize()
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.f.seek(0)
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.f:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax = float(parts[1])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
+        rows = self._rows()
+        inside = [r for r in rows if self.t0 <= r[0] <= self.t1]
+        used = inside
+        if not used:
+            before = [r for r in rows if r[0] < self.t0][-1:]
+            after = [r for r in rows if r[0] > self.t1][:1]
+            used = before + after
+        reasons = set()
+        for r in used:
+            for n, v in zip(self.NAMES, r[3]):
                 if v.lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        sm = [r[1] for r in used]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": used[-1][2] if used else None, "reasons": sorted(reasons),
+                "samples_in_region": len(inside), "samples_used": len(used)}
 
 
 def dist_init():
@@ -248,8 +294,10 @@ def run_ours(args, rank, world, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     with ClockSampler(local) as clk:
+        clk.settle(step)                          # a sample under load exists before the region
         barrier(world)
         torch.cuda.synchronize()
+        clk.mark_start()
         t0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(float(i))                 # evict L2 between steps (not timed)
@@ -259,6 +307,9 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - t0
+        clk.mark_end()
+        clk.settle(step, after=clk.t1)            # and one after it
+        clocks = clk.summary()
     assert int(err.item()) == 0, f"device error flag {int(err.item())}"
     times_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = sum(times_ms) / 1e3
@@ -312,7 +363,7 @@ def run_ours(args, rank, world, local):
                      "traffic": traffic, "kernel": "decode_paged_kernel (+ merge_splits_kernel inside the same events)"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "q, block_table and kv_lens copied in from pinned host memory and out, lse copied back every step; the KV page pool is resident device state"},
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
         "wall_s": wall,
     }
@@ -368,7 +419,7 @@ def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -343,12 +343,17 @@ decode_paged_kernel(const DecodeArgs a) {
               for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
               const bool hi = mx > ref[gi] + beta2;
               const bool lo = first_chunk && mx < ref[gi] - beta2;
-              if (hi || lo) {
+              if (hi) {
+                // Raise the reference and shrink what was accumulated against the old one.
                 const float alpha = ex2(ref[gi] - mx);
-                ref[gi] = mx;
                 lsum[gi] *= alpha;
 #pragma unroll
                 for (int e = 0; e < C::DPL; ++e) acc[gi][e] *= alpha;
+              }
+              if (hi || lo) {
+                // A lowered reference (first chunk only) has nothing accumulated to rescale;
+                // ex2(old - new) would overflow there.
+                ref[gi] = mx;
                 ++fallbacks;
               }
             }
@@ -424,7 +429,10 @@ decode_paged_kernel(const DecodeArgs a) {
     if (lane == 0) {
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
-        cref[warp * G + gi] = ref[gi];
+        // A warp that accumulated nothing must not set the common reference:
+        // in the unified variant its reference is still phi, which may sit far
+        // above every real logit.
+        cref[warp * G + gi] = lsum[gi] > 0.0f ? ref[gi] : -INFINITY;
         cl[warp * G + gi] = lsum[gi];
       }
       if constexpr (UNIFIED) {
