@@ -37,6 +37,14 @@ METRIC = "paged decode-attn HBM GB/s (% of peak); causal prefill attn TFLOP/s (%
 WORKLOAD = ("llama7b_batched_decode: bf16, batch 16, 32 query heads = 32 KV heads, head_dim 128, "
             "kv_len U[512,4096] seeded, page_size 16, 8192-page pool, one query token per sequence")
 PREFILL_WORKLOAD = "causal_prefill_llama7b: bf16, batch 8, T 1024, 32/32 heads, head_dim 128, [B,T,H,D]"
+# decode workloads: (builder name, description, explicit split count or 0 for automatic)
+DECODE_WORKLOADS = {
+    "llama7b_batched_decode": ("llama7b_batched_decode", WORKLOAD, 0),
+    "long_context_gqa_decode": ("long_context_gqa_decode",
+                                "long_context_gqa_decode: bf16, batch 4, 32 query heads over 8 KV heads, "
+                                "head_dim 128, kv_len 32768, page_size 16, 8192-page shuffled pool, 32 KV splits",
+                                32),
+}
 FALLBACK_HBM = 6800.0
 FALLBACK_BF16 = 1900.0
 L2_FLUSH_BYTES = 256 << 20
@@ -261,7 +269,14 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
 
-    case = workloads.llama7b_batched_decode(poison=False)
+    stream = torch.cuda.current_stream(dev)
+    if args.only == "prefill":
+        pre = prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "only": "prefill", "prefill": pre}), flush=True)
+        return
+    builder, workload_desc, req_splits = DECODE_WORKLOADS[args.workload]
+    case = getattr(workloads, builder)(poison=False)
     cpu_rate = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_rate = oracle_decode_rate(case, budget_s=12.0)
@@ -272,19 +287,19 @@ def run_ours(args, rank, world, local):
     bt = case.block_table.to(dev)
     lens = case.kv_lens.to(dev)
     B_, Hq, D = case.q.shape
-    S = B.decode_num_splits(B_, case.max_blocks, Hq, case.n_kv_heads, D, case.page_size, 0)
+    S = B.decode_num_splits(B_, case.max_blocks, Hq, case.n_kv_heads, D, case.page_size, req_splits,
+                            B.PKV_BF16)
     ws = B.alloc_workspace(B.decode_workspace_size(B_, case.max_blocks, Hq, case.n_kv_heads, D,
-                                                   case.page_size, 0), dev)
+                                                   case.page_size, req_splits, B.PKV_BF16), dev)
     out = torch.empty_like(q)
     lse = torch.empty(B_, Hq, dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
     launches_per_step = 1 + (1 if S > 1 else 0)
     algo_bytes = case.kv_bytes()
 
     def step():
-        B.decode_paged(q, kp, vp, bt, lens, case.scale, num_splits=0, out=out, lse=lse,
+        B.decode_paged(q, kp, vp, bt, lens, case.scale, num_splits=req_splits, out=out, lse=lse,
                        workspace=ws, err_flag=err)
 
     for _ in range(max(3, args.warmup)):
@@ -348,15 +363,14 @@ def run_ours(args, rank, world, local):
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
     units = int(case.kv_lens.sum())
-    traffic = profiled_traffic("decode_llama7b_batched", source_hash("decode_kernel.cuh", "decode.cu"),
-                               units)
+    traffic = profiled_traffic(args.workload, source_hash("decode_kernel.cuh", "decode.cu"), units)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}", "num_splits": S,
+        "config": {"workload": workload_desc, "parallelism": f"replicas{world}", "num_splits": S,
                    "algorithmic_bytes_per_step": algo_bytes,
-                   "l2": "inputs (604 MB of K/V) exceed the 129 MB L2, and a 256 MiB buffer is written between timed steps",
+                   "l2": f"inputs ({algo_bytes / 1e6:.0f} MB of K/V) exceed the 129 MB L2, and a 256 MiB buffer is written between timed steps",
                    "timing": "CUDA events around each call on the launch stream; sum over steps; max over ranks"},
         "roofline": {"bound": "hbm", "achieved": kernel_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": kernel_gbs / hbm_peak, "peak_source": f"{peak_src} hbm_gbs",
@@ -372,7 +386,9 @@ def run_ours(args, rank, world, local):
                                 "sample": f"{cpu_rate[1]} whole pass(es) of the fp64 oracle over the same decode batch in {cpu_rate[2]:.1f} s"}
 
     # ---- causal prefill on the same line (its own roofline against dense bf16)
-    pre = prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src)
+    pre = None
+    if args.only == "all":
+        pre = prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src)
     if pre is not None:
         line["prefill"] = pre
         line["gpu_launches"] += pre.pop("launches")
@@ -423,6 +439,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+                    help="run one part only (for profiler captures)")
+    ap.add_argument("--workload", choices=sorted(DECODE_WORKLOADS), default="llama7b_batched_decode",
+                    help="decode workload of the timed step (the headline is llama7b_batched_decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -79,17 +79,23 @@ extern "C" {
 /* Human-readable name of a status code. Static storage; never NULL. */
 const char* attn_status_string(int status);
 
+/* Text of the CUDA error behind the most recent PKV_ERR_LAUNCH returned on the
+ * calling host thread ("no error" if there was none). Static storage; never NULL.
+ * A diagnostic for callers; the pages define no counterpart. */
+const char* attn_last_cuda_error_string(void);
+
 /*
- * Number of KV splits the decode calls use for this shape. num_splits > 0 is
- * taken as asked (capped at max_blocks_per_seq); 0 lets the library choose from
- * the shape and the SM count of the current device. A split covers a contiguous
+ * Number of KV splits the decode calls use for this shape and dtype. num_splits > 0
+ * is taken as asked (capped at max_blocks_per_seq); 0 lets the library choose from
+ * the shape, the SM count of the current device and how many decode CTAs fit on an
+ * SM, as the split count that minimises (waves of CTAs) x (pages per CTA + 4). A split covers a contiguous
  * range of ceil(max_blocks_per_seq / splits) pages of a sequence.
  * FlashDecoding computes each partial softmax independently and combines them
  * all at the end ("【FlashAttention-V4，非官方】FlashDecoding++", section 1).
  * Returns the split count (>= 1) or a negative PKV_ERR_* code.
  */
 int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, int n_kv_heads,
-                           int head_dim, int page_size, int num_splits);
+                           int head_dim, int page_size, int num_splits, int dtype);
 
 /*
  * Workspace bytes attn_decode_paged and attn_decode_paged_unified_max need for
@@ -98,7 +104,8 @@ int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, in
  * (size_t)-1 for invalid arguments.
  */
 size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_heads,
-                                  int n_kv_heads, int head_dim, int page_size, int num_splits);
+                                  int n_kv_heads, int head_dim, int page_size, int num_splits,
+                                  int dtype);
 
 /*
  * Single-token decode over a paged KV cache.

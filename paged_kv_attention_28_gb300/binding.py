@@ -29,7 +29,7 @@ PKV_DEVERR_BAD_LEN = 2
 PKV_DEVERR_TIMEOUT = 4
 
 EXPORTS = [
-    "attn_status_string", "attn_decode_num_splits", "attn_decode_workspace_size",
+    "attn_status_string", "attn_last_cuda_error_string", "attn_decode_num_splits", "attn_decode_workspace_size",
     "attn_decode_paged", "attn_decode_paged_unified_max", "attn_merge_states",
     "attn_prefill_causal", "attn_cascade_workspace_size", "attn_decode_cascade",
 ]
@@ -37,7 +37,10 @@ EXPORTS = [
 
 class AttnError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: {status_string(status)} ({status})")
+        msg = f"{what}: {status_string(status)} ({status})"
+        if status == PKV_ERR_LAUNCH:
+            msg += f": {lib.attn_last_cuda_error_string().decode()}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -50,10 +53,12 @@ def _load() -> ctypes.CDLL:
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_status_string.argtypes = [i32]
+    lib.attn_last_cuda_error_string.restype = ctypes.c_char_p
+    lib.attn_last_cuda_error_string.argtypes = []
     lib.attn_decode_num_splits.restype = i32
-    lib.attn_decode_num_splits.argtypes = [i32] * 7
+    lib.attn_decode_num_splits.argtypes = [i32] * 8
     lib.attn_decode_workspace_size.restype = sz
-    lib.attn_decode_workspace_size.argtypes = [i32] * 7
+    lib.attn_decode_workspace_size.argtypes = [i32] * 8
     lib.attn_decode_paged.restype = i32
     lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [i32] * 7 + [f32, i32, i32, vp, sz, vp, vp]
     lib.attn_decode_paged_unified_max.restype = i32
@@ -113,17 +118,18 @@ def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
 
 # --------------------------------------------------------------------------- decode
 
-def decode_num_splits(batch, max_blocks, n_qo_heads, n_kv_heads, head_dim, page_size, num_splits=0):
+def decode_num_splits(batch, max_blocks, n_qo_heads, n_kv_heads, head_dim, page_size, num_splits=0,
+                      dtype=PKV_BF16):
     r = lib.attn_decode_num_splits(batch, max_blocks, n_qo_heads, n_kv_heads, head_dim, page_size,
-                                   num_splits)
+                                   num_splits, dtype)
     _check(min(r, 0), "attn_decode_num_splits")
     return r
 
 
 def decode_workspace_size(batch, max_blocks, n_qo_heads, n_kv_heads, head_dim, page_size,
-                          num_splits=0) -> int:
+                          num_splits=0, dtype=PKV_BF16) -> int:
     n = lib.attn_decode_workspace_size(batch, max_blocks, n_qo_heads, n_kv_heads, head_dim,
-                                       page_size, num_splits)
+                                       page_size, num_splits, dtype)
     if n == ctypes.c_size_t(-1).value:
         raise AttnError(PKV_ERR_INVALID_ARG, "attn_decode_workspace_size")
     return n
@@ -154,7 +160,7 @@ def decode_paged(q, k_pages, v_pages, block_table, kv_lens, scale, num_splits=0,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    ws_bytes = decode_workspace_size(B, max_blocks, Hq, Hkv, D, P, num_splits)
+    ws_bytes = decode_workspace_size(B, max_blocks, Hq, Hkv, D, P, num_splits, _dt(q))
     if workspace is None:
         workspace = alloc_workspace(ws_bytes, q.device)
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()

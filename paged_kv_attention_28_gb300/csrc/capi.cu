@@ -7,6 +7,14 @@
 
 namespace pkv {
 
+static thread_local cudaError_t g_last_error = cudaSuccess;
+
+int check_launch(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  g_last_error = e;
+  return PKV_ERR_LAUNCH;
+}
+
 int device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -18,23 +26,31 @@ int device_sm_count() {
   return n;
 }
 
-SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested) {
+SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested,
+                             int ctas_per_sm) {
   int S;
   if (requested > 0) {
     S = requested < max_blocks ? requested : max_blocks;
   } else {
-    // Enough CTAs for several waves on every SM if each sequence were full length,
-    // but never splits shorter than 16 pages.
-    const long units = (long)batch * n_kv_heads;
+    // Model the time of a split count as (waves of CTAs) x (pages per CTA + a fixed
+    // per-CTA cost of about 4 pages), assuming every sequence is full length, and
+    // take the cheapest. This favours splits that fill whole waves of resident CTAs.
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
-    const long target = 4L * sms;
-    long s = (target + units - 1) / units;
-    long max_s = max_blocks / 16;
-    if (max_s < 1) max_s = 1;
-    if (s > max_s) s = max_s;
-    if (s < 1) s = 1;
-    S = (int)s;
+    const long slots = (long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+    const long units = (long)batch * n_kv_heads;
+    const int s_max = max_blocks < 64 ? max_blocks : 64;
+    long best_cost = -1;
+    S = 1;
+    for (int s = 1; s <= s_max; ++s) {
+      const long pps = (max_blocks + s - 1) / s;
+      const long waves = (units * s + slots - 1) / slots;
+      const long cost = waves * (pps + 4);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        S = s;
+      }
+    }
   }
   const int pps = (max_blocks + S - 1) / S;
   return SplitPlan{(max_blocks + pps - 1) / pps, pps};
@@ -79,7 +95,8 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   const int G = c.n_qo_heads / c.n_kv_heads;
   if (!decode_supported(c.dtype, c.head_dim, c.page_size, G)) return PKV_ERR_UNSUPPORTED;
   if (c.batch > 65535 || c.n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-  const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, c.n_kv_heads, c.num_splits);
+  const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, c.n_kv_heads, c.num_splits,
+                                            decode_ctas_per_sm(c.dtype, c.head_dim, G));
   const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.head_dim, plan.num_splits);
   if (need > 0 && (!c.workspace || c.workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(c.workspace) & 255u) != 0))
@@ -137,18 +154,26 @@ const char* attn_status_string(int status) {
   }
 }
 
+const char* attn_last_cuda_error_string(void) {
+  return g_last_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_error);
+}
+
 int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, int n_kv_heads,
-                           int head_dim, int page_size, int num_splits) {
+                           int head_dim, int page_size, int num_splits, int dtype) {
   if (batch < 0 || max_blocks_per_seq < 1 || n_qo_heads < 1 || n_kv_heads < 1 ||
       head_dim < 1 || page_size < 1 || num_splits < 0 || n_qo_heads % n_kv_heads)
     return PKV_ERR_INVALID_ARG;
-  return plan_decode_splits(batch, max_blocks_per_seq, n_kv_heads, num_splits).num_splits;
+  if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  return plan_decode_splits(batch, max_blocks_per_seq, n_kv_heads, num_splits,
+                            decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads))
+      .num_splits;
 }
 
 size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_heads,
-                                  int n_kv_heads, int head_dim, int page_size, int num_splits) {
+                                  int n_kv_heads, int head_dim, int page_size, int num_splits,
+                                  int dtype) {
   const int S = attn_decode_num_splits(batch, max_blocks_per_seq, n_qo_heads, n_kv_heads,
-                                       head_dim, page_size, num_splits);
+                                       head_dim, page_size, num_splits, dtype);
   if (S < 0) return (size_t)-1;
   return decode_ws_bytes(batch, n_qo_heads, head_dim, S);
 }

@@ -57,7 +57,7 @@ template <typename T, int D>
 int launch_merge_t(const DecodeArgs& a, cudaStream_t stream) {
   const int rows = a.batch * a.n_qo_heads;
   merge_splits_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+  return check_launch(cudaGetLastError());
 }
 
 int launch_merge_splits(const DecodeArgs& a, cudaStream_t stream) {
@@ -72,6 +72,28 @@ int launch_merge_splits(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 int dispatch_decode_unified(const DecodeArgs& a, cudaStream_t stream);  // decode_um.cu
+
+int decode_ctas_per_sm(int dtype, int head_dim, int group) {
+#define PKV_CPS(TT)                                                            \
+  if (head_dim == 64) {                                                        \
+    if (group == 1) return ctas_per_sm_t<TT, 64, 1>();                         \
+    if (group == 2) return ctas_per_sm_t<TT, 64, 2>();                         \
+    if (group == 4) return ctas_per_sm_t<TT, 64, 4>();                         \
+    if (group == 8) return ctas_per_sm_t<TT, 64, 8>();                         \
+  } else {                                                                     \
+    if (group == 1) return ctas_per_sm_t<TT, 128, 1>();                        \
+    if (group == 2) return ctas_per_sm_t<TT, 128, 2>();                        \
+    if (group == 4) return ctas_per_sm_t<TT, 128, 4>();                        \
+    if (group == 8) return ctas_per_sm_t<TT, 128, 8>();                        \
+  }
+  if (dtype == PKV_F32) {
+    PKV_CPS(float)
+  } else {
+    PKV_CPS(__nv_bfloat16)
+  }
+#undef PKV_CPS
+  return 2;
+}
 
 bool decode_supported(int dtype, int head_dim, int page_size, int group) {
   return (dtype == PKV_F32 || dtype == PKV_BF16) && (head_dim == 64 || head_dim == 128) &&
@@ -121,7 +143,7 @@ int launch_merge_pair(const float* out_a, const float* lse_a, const float* out_b
   else
     merge_pair_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(
         out_a, lse_a, out_b, lse_b, static_cast<__nv_bfloat16*>(out), lse, n_rows, head_dim);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+  return check_launch(cudaGetLastError());
 }
 
 }  // namespace pkv

@@ -59,12 +59,29 @@ struct DecodeCfg {
   static constexpr int BAR_OFF = 2 * NSTAGE * TILE;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NSTAGE * 8;
   static constexpr int SMEM = FLAG_OFF + 16;
-  static_assert(D % LPT == 0 && DPL % VEC == 0, "head_dim split");
+  static_assert(D % LPT == 0 && DPL % VEC == 0 && VEC % 2 == 0, "head_dim split");
   static_assert(P % TPI == 0 && ITERS % NIT == 0, "page split");
   static_assert(NSTAGE % NW == 0, "stage ownership");
   static_assert(TILE % 16 == 0, "bulk copy granularity");
   static_assert(NW * G * (D + 2) * 4 <= 2 * NSTAGE * TILE, "combine scratch fits in the ring");
 };
+
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+// Two independent fp32 fused multiply-adds in one instruction (sm_100 family).
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 
 struct DecodeFlags {
   int abort_;
@@ -73,34 +90,30 @@ struct DecodeFlags {
   int fallbacks;
 };
 
+// Loads VEC elements of one K or V row from shared memory (VEC * sizeof(T)
+// bytes, aligned) as VEC/2 packed (even, odd) fp32 pairs. bf16 -> fp32 is a
+// 16-bit left shift of the bit pattern.
 template <typename T, int VEC>
-__device__ __forceinline__ void load_row_vec(const T* p, float* f) {
+__device__ __forceinline__ void load_row_pairs(const T* p, uint64_t* f2) {
   if constexpr (sizeof(T) == 4) {
-    static_assert(VEC == 4 || VEC == 2, "fp32 vector");
     if constexpr (VEC == 4) {
       const float4 x = *reinterpret_cast<const float4*>(p);
-      f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+      f2[0] = pk2(x.x, x.y);
+      f2[1] = pk2(x.z, x.w);
     } else {
       const float2 x = *reinterpret_cast<const float2*>(p);
-      f[0] = x.x; f[1] = x.y;
+      f2[0] = pk2(x.x, x.y);
     }
   } else {
-    static_assert(VEC == 8 || VEC == 4, "bf16 vector");
-    // bf16 -> fp32 is a 16-bit left shift of the bit pattern.
     if constexpr (VEC == 8) {
       const uint4 x = *reinterpret_cast<const uint4*>(p);
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-      }
+      for (int i = 0; i < 4; ++i) f2[i] = pk2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
     } else {
       const uint2 x = *reinterpret_cast<const uint2*>(p);
-      f[0] = __uint_as_float(x.x << 16);
-      f[1] = __uint_as_float(x.x & 0xffff0000u);
-      f[2] = __uint_as_float(x.y << 16);
-      f[3] = __uint_as_float(x.y & 0xffff0000u);
+      f2[0] = pk2(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
+      f2[1] = pk2(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
     }
   }
 }
@@ -232,18 +245,20 @@ decode_paged_kernel(const DecodeArgs a) {
   // ---------------------------------------------------------------- consumer warps
   const int tg = lane / C::LPT;  // token row within a step
   const int j = lane % C::LPT;   // column group within the row
-  float ref[G], lsum[G], acc[G][C::DPL];
+  constexpr int DP2 = C::DPL / 2;  // packed pairs per lane
+  float ref[G], lsum[G];
+  uint64_t acc2[G][DP2];
 #pragma unroll
   for (int gi = 0; gi < G; ++gi) {
     ref[gi] = UNIFIED ? a.phi * kLog2e : -INFINITY;
     lsum[gi] = 0.0f;
 #pragma unroll
-    for (int e = 0; e < C::DPL; ++e) acc[gi][e] = 0.0f;
+    for (int e = 0; e < DP2; ++e) acc2[gi][e] = 0ull;  // (+0, +0)
   }
   int fallbacks = 0;
 
   if (warp < C::NW) {
-    float qr[G][C::DPL];
+    uint64_t q2[G][DP2];
     const float qscale = a.scale * kLog2e;
     const T* qp = static_cast<const T*>(a.q) + ((size_t)b * a.n_qo_heads + g * G) * D;
 #pragma unroll
@@ -251,8 +266,10 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int c = 0; c < C::NV; ++c)
 #pragma unroll
-        for (int e = 0; e < C::VEC; ++e)
-          qr[gi][c * C::VEC + e] = to_f32<T>(qp[gi * D + c * C::LPT * C::VEC + j * C::VEC + e]) * qscale;
+        for (int e = 0; e < C::VEC; e += 2) {
+          const T* src = qp + gi * D + c * C::LPT * C::VEC + j * C::VEC + e;
+          q2[gi][(c * C::VEC + e) / 2] = pk2(to_f32<T>(src[0]) * qscale, to_f32<T>(src[1]) * qscale);
+        }
 
     const float beta2 = kUnifiedBeta * kLog2e;
     bool first_chunk = true;
@@ -274,19 +291,17 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int it = 0; it < C::NIT; ++it) {
           const int t = (ch * C::NIT + it) * C::TPI + tg;
-          float kf[C::DPL];
+          uint64_t k2[DP2];
 #pragma unroll
           for (int c = 0; c < C::NV; ++c)
-            load_row_vec<T, C::VEC>(kt + t * D + c * C::LPT * C::VEC + j * C::VEC, kf + c * C::VEC);
+            load_row_pairs<T, C::VEC>(kt + t * D + c * C::LPT * C::VEC + j * C::VEC, k2 + c * C::VEC / 2);
 #pragma unroll
           for (int gi = 0; gi < G; ++gi) {
-            float d0 = 0.0f, d1 = 0.0f;
+            uint64_t d2 = 0ull;
 #pragma unroll
-            for (int e = 0; e < C::DPL; e += 2) {
-              d0 = fmaf(qr[gi][e], kf[e], d0);
-              d1 = fmaf(qr[gi][e + 1], kf[e + 1], d1);
-            }
-            sc[it][gi] = d0 + d1;
+            for (int e = 0; e < DP2; ++e) d2 = ffma2(q2[gi][e], k2[e], d2);
+            const float2 d = upk2(d2);
+            sc[it][gi] = d.x + d.y;
           }
         }
 #pragma unroll
@@ -314,10 +329,11 @@ decode_paged_kernel(const DecodeArgs a) {
             for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             if (mx > ref[gi]) {  // warp-uniform: every lane holds the same mx and ref
               const float alpha = ex2(ref[gi] - mx);
+              const uint64_t al2 = pk2(alpha, alpha);
               ref[gi] = mx;
               lsum[gi] *= alpha;
 #pragma unroll
-              for (int e = 0; e < C::DPL; ++e) acc[gi][e] *= alpha;
+              for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(acc2[gi][e], al2, 0ull);
             }
           }
         } else {
@@ -346,9 +362,10 @@ decode_paged_kernel(const DecodeArgs a) {
               if (hi) {
                 // Raise the reference and shrink what was accumulated against the old one.
                 const float alpha = ex2(ref[gi] - mx);
+                const uint64_t al2 = pk2(alpha, alpha);
                 lsum[gi] *= alpha;
 #pragma unroll
-                for (int e = 0; e < C::DPL; ++e) acc[gi][e] *= alpha;
+                for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(acc2[gi][e], al2, 0ull);
               }
               if (hi || lo) {
                 // A lowered reference (first chunk only) has nothing accumulated to rescale;
@@ -371,15 +388,17 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int it = 0; it < C::NIT; ++it) {
           const int t = (ch * C::NIT + it) * C::TPI + tg;
-          float vf[C::DPL];
+          uint64_t v2[DP2];
 #pragma unroll
           for (int c = 0; c < C::NV; ++c)
-            load_row_vec<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, vf + c * C::VEC);
+            load_row_pairs<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
           if (t < valid) {
 #pragma unroll
-            for (int gi = 0; gi < G; ++gi)
+            for (int gi = 0; gi < G; ++gi) {
+              const uint64_t p2 = pk2(sc[it][gi], sc[it][gi]);
 #pragma unroll
-              for (int e = 0; e < C::DPL; ++e) acc[gi][e] = fmaf(sc[it][gi], vf[e], acc[gi][e]);
+              for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+            }
           }
         }
       }
@@ -394,7 +413,12 @@ decode_paged_kernel(const DecodeArgs a) {
       for (int gi = 0; gi < G; ++gi) {
         lsum[gi] += __shfl_xor_sync(0xffffffffu, lsum[gi], off);
 #pragma unroll
-        for (int e = 0; e < C::DPL; ++e) acc[gi][e] += __shfl_xor_sync(0xffffffffu, acc[gi][e], off);
+        for (int e = 0; e < DP2; ++e) {
+          float2 v = upk2(acc2[gi][e]);
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
+          acc2[gi][e] = pk2(v.x, v.y);
+        }
       }
   }
 
@@ -445,8 +469,11 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int c = 0; c < C::NV; ++c)
 #pragma unroll
-          for (int e = 0; e < C::VEC; ++e)
-            cacc[(warp * G + gi) * D + c * C::LPT * C::VEC + j * C::VEC + e] = acc[gi][c * C::VEC + e];
+          for (int e = 0; e < C::VEC; e += 2) {
+            const float2 v = upk2(acc2[gi][(c * C::VEC + e) / 2]);
+            cacc[(warp * G + gi) * D + c * C::LPT * C::VEC + j * C::VEC + e] = v.x;
+            cacc[(warp * G + gi) * D + c * C::LPT * C::VEC + j * C::VEC + e + 1] = v.y;
+          }
     }
   }
   __syncthreads();
@@ -495,13 +522,20 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 32 && !(configured_mask & (1 << dev))) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    if (check_launch(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM)) != PKV_OK)
       return PKV_ERR_LAUNCH;
     configured_mask |= (1 << dev);
   }
   dim3 grid(a.num_splits, a.n_kv_heads, a.batch);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+  return check_launch(cudaGetLastError());
+}
+
+template <typename T, int D, int G>
+constexpr int ctas_per_sm_t() {
+  using C = DecodeCfg<T, D, 16, G>;
+  constexpr int by_smem = (227 * 1024) / C::SMEM;
+  return by_smem < C::MIN_BLOCKS ? by_smem : C::MIN_BLOCKS;
 }
 
 template <bool UNIFIED>

@@ -37,7 +37,15 @@ struct SplitPlan {
 };
 
 int device_sm_count();
-SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested);
+
+// Remembers the most recent failing CUDA call of this host thread (see
+// attn_last_cuda_error_string) and returns PKV_ERR_LAUNCH, or PKV_OK on success.
+int check_launch(cudaError_t e);
+// Split count and pages per split. `ctas_per_sm` is how many decode CTAs of the
+// dispatched instantiation fit on one SM (decode_ctas_per_sm).
+SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested,
+                             int ctas_per_sm);
+int decode_ctas_per_sm(int dtype, int head_dim, int group);
 
 // Enqueues the decode kernel (and the merge kernel when num_splits > 1).
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);

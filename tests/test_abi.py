@@ -49,14 +49,23 @@ def test_split_planning(b):
     assert b.decode_num_splits(1, 10, 8, 8, 64, 16, 3) == 3
     # 10 pages in 4 splits -> 3 pages per split -> 4 splits
     assert b.decode_num_splits(1, 10, 8, 8, 64, 16, 4) == 4
-    # automatic choice: at least one split, never splits below 16 pages
-    s = b.decode_num_splits(16, 256, 32, 32, 128, 16, 0)
-    assert 1 <= s <= 16
-    assert b.decode_num_splits(1, 16, 8, 8, 64, 16, 0) == 1
+    # automatic choice: between 1 and 64 splits, at most one per page
+    for args in [(16, 256, 32, 32, 128, 16), (1, 16, 8, 8, 64, 16), (4, 2048, 32, 8, 128, 16),
+                 (64, 8, 8, 8, 64, 16)]:
+        s = b.decode_num_splits(*args, 0)
+        assert 1 <= s <= min(64, args[1])
+    # a large batch of long sequences already fills the GPU: few splits
+    assert b.decode_num_splits(512, 256, 32, 32, 128, 16, 0) <= 2
 
 
 def test_workspace_size(b):
     assert b.decode_workspace_size(1, 16, 8, 8, 64, 16, 1) == 0
+    # the query and the planner agree for both dtypes
+    for dt in (b.PKV_F32, b.PKV_BF16):
+        s = b.decode_num_splits(16, 256, 32, 32, 128, 16, 0, dt)
+        n = b.decode_workspace_size(16, 256, 32, 32, 128, 16, 0, dt)
+        rows = 16 * 32
+        assert n == (0 if s == 1 else rows * s * 128 * 4 + ((rows * s * 4 + 255) // 256) * 256)
     n = b.decode_workspace_size(4, 2048, 32, 8, 128, 16, 32)
     rows = 4 * 32
     assert n == rows * 32 * 128 * 4 + ((rows * 32 * 4 + 255) // 256) * 256
