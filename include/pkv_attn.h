@@ -132,6 +132,43 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                       void* stream);
 
 /*
+ * Allocation-free variant of attn_decode_paged (the pages have no counterpart;
+ * this is a convenience of the library).
+ *
+ * Some callers cannot allocate device memory when they call in. Examples are an
+ * inference runtime's plugin or enqueue hook that is not allowed to allocate
+ * while it runs, and a process that reserved all device memory up front for its
+ * own pool. Those callers cannot supply the workspace that attn_decode_paged
+ * wants. This entry point keeps the split partial states in a scratch array
+ * that the library owns instead: PKV_NOALLOC_SCRATCH_BYTES bytes of static
+ * device memory, held on every GPU that loads the library until the process
+ * exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * - Arguments, layouts and results are those of attn_decode_paged, minus the
+ *   workspace. The output equals attn_decode_paged's for the same split count.
+ * - Returns PKV_ERR_WORKSPACE when the shape needs more than
+ *   PKV_NOALLOC_SCRATCH_BYTES of partial states, i.e. when
+ *   attn_decode_workspace_size(...) > PKV_NOALLOC_SCRATCH_BYTES. Fewer splits
+ *   (num_splits) or a smaller batch fit.
+ * - The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress) with that device current, and caches it. Make that
+ *   first call before any stream capture on that device.
+ * - Every call on a device shares the one array. Calls whose kernels overlap on
+ *   the GPU (different streams, no ordering between them) race on it and give
+ *   wrong results; order them, e.g. on one stream. The array keeps the last
+ *   call's contents. Nothing in it needs to start at zero: every partial state
+ *   that a call reads was written by the same call.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB of fp32 partial states */
+
+int attn_decode_paged_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* block_table, const int32_t* kv_lens, void* out,
+                              float* lse, int batch, int max_blocks_per_seq, int num_pages,
+                              int n_qo_heads, int n_kv_heads, int head_dim, int page_size,
+                              float scale, int num_splits, int dtype, int32_t* err_flag,
+                              void* stream);
+
+/*
  * Decode with FlashDecoding++'s asynchronised softmax with a unified maximum
  * value ("【FlashAttention-V4，非官方】FlashDecoding++", sections 1 and 3).
  * Scaled logits are exponentiated against the preset value `phi` (natural-log

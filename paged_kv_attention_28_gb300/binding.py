@@ -32,6 +32,7 @@ EXPORTS = [
     "attn_status_string", "attn_last_cuda_error_string", "attn_decode_num_splits", "attn_decode_workspace_size",
     "attn_decode_paged", "attn_decode_paged_unified_max", "attn_merge_states",
     "attn_prefill_causal", "attn_cascade_workspace_size", "attn_decode_cascade",
+    "attn_decode_paged_noalloc",
 ]
 
 
@@ -64,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_decode_paged_unified_max.restype = i32
     lib.attn_decode_paged_unified_max.argtypes = ([vp, vp, vp, vp, vp, vp, vp] + [i32] * 7 +
                                                   [f32, i32, i32, f32, vp, vp, sz, vp, vp])
+    lib.attn_decode_paged_noalloc.restype = i32
+    lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [i32] * 7 + [f32, i32, i32, vp, vp]
     lib.attn_merge_states.restype = i32
     lib.attn_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]
     lib.attn_prefill_causal.restype = i32
