@@ -392,8 +392,79 @@ def run_ours(args, rank, world, local):
     if pre is not None:
         line["prefill"] = pre
         line["gpu_launches"] += pre.pop("launches")
+    if args.only == "all" and args.workload == "llama7b_batched_decode":
+        line["also"] = other_workloads(B, workloads, dev, stream, min(args.steps, 200), hbm_peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_calls(fn, steps, stream, dev):
+    """Mean device time (ms) of ``fn`` over ``steps`` calls, L2 flushed before each call."""
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def other_workloads(B, workloads, dev, stream, steps, hbm_peak):
+    """The remaining workloads, each timed on its own: GB/s of algorithmic K/V bytes."""
+    res = {}
+
+    def entry(name, nbytes, ms, extra=None):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        d = {"value": gbs, "unit": "GB/s", "ms_per_call": ms, "algorithmic_bytes": nbytes,
+             "frac_of_measured_hbm": gbs / hbm_peak}
+        if extra:
+            d.update(extra)
+        res[name] = d
+
+    c = workloads.long_context_gqa_decode(poison=False)
+    q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
+    out = torch.empty_like(q)
+    lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
+    S = workloads.LONG_CONTEXT_SPLITS
+    ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads,
+                                                   c.n_kv_heads, c.head_dim, 16, S, B.PKV_BF16), dev)
+    ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
+                                           lse=lse, workspace=ws), steps, stream, dev)
+    entry("long_context_gqa_decode", c.kv_bytes(), ms, {"num_splits": S})
+    fb = torch.zeros(1, dtype=torch.int32, device=dev)
+    ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
+                                           lse=lse, workspace=ws, unified_phi=0.0,
+                                           fallback_count=fb), steps, stream, dev)
+    entry("long_context_gqa_decode_unified_max", c.kv_bytes(), ms,
+          {"num_splits": S, "phi": 0.0, "fallbacks_total": int(fb.item())})
+    del q, kp, vp, bt, ln, ws
+
+    c = workloads.cascade_shared_prefix_decode(poison=False)
+    q, kp, vp, pt, st, sl = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.prefix_table,
+                                                 c.suffix_table, c.suffix_lens))
+    out = torch.empty_like(q)
+    lse = torch.empty(c.n_requests, c.n_qo_heads, dtype=torch.float32, device=dev)
+    ws = B.alloc_workspace(B.cascade_workspace_size(c.n_requests, c.prefix_len, st.shape[1],
+                                                    c.n_qo_heads, c.n_kv_heads, c.head_dim,
+                                                    c.page_size), dev)
+    ms = time_calls(lambda: B.decode_cascade(q, kp, vp, pt, c.prefix_len, st, sl, c.scale, out=out,
+                                             lse=lse, workspace=ws), steps, stream, dev)
+    entry("cascade_shared_prefix_decode", c.kv_bytes(), ms,
+          {"bytes_note": "shared prefix K/V counted once plus every suffix"})
+    del q, kp, vp, pt, st, sl, ws
+
+    c = workloads.single_seq_decode_f32()
+    q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
+    ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale), steps, stream, dev)
+    entry("single_seq_decode_f32", c.kv_bytes(), ms,
+          {"note": "1 MiB of K/V: launch-latency bound; L2 flushed before each call"})
+    return res
 
 
 def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src):

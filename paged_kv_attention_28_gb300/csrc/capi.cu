@@ -236,9 +236,11 @@ size_t attn_cascade_workspace_size(int n_requests, int prefix_len, int max_suffi
       n_kv_heads < 1 || head_dim < 1 || page_size < 1 || n_qo_heads % n_kv_heads)
     return (size_t)-1;
   const size_t rows = (size_t)n_requests * n_qo_heads;
-  const int chunks = cascade_prefix_chunks(prefix_len, n_requests, n_qo_heads, n_kv_heads);
+  const int chunks = cascade_prefix_chunks(prefix_len, page_size, n_requests, n_qo_heads, n_kv_heads);
+  const SplitPlan suf = cascade_suffix_plan(n_requests, max_suffix_blocks, n_qo_heads, n_kv_heads,
+                                            head_dim, PKV_BF16);
   return align_up((size_t)chunks * rows * head_dim * 4, 256) + align_up((size_t)chunks * rows * 4, 256) +
-         align_up(rows * head_dim * 4, 256) + align_up(rows * 4, 256);
+         align_up(rows * suf.num_splits * head_dim * 4, 256) + align_up(rows * suf.num_splits * 4, 256);
 }
 
 int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
@@ -287,14 +289,18 @@ int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
   a.dtype = dtype;
   a.err_flag = err_flag;
   const size_t rows = (size_t)n_requests * n_qo_heads;
-  a.prefix_chunks = cascade_prefix_chunks(prefix_len, n_requests, n_qo_heads, n_kv_heads);
+  a.prefix_chunks = cascade_prefix_chunks(prefix_len, page_size, n_requests, n_qo_heads, n_kv_heads);
+  const SplitPlan suf = cascade_suffix_plan(n_requests, max_suffix_blocks, n_qo_heads, n_kv_heads,
+                                            head_dim, PKV_BF16);
+  a.suffix_splits = suf.num_splits;
+  a.suffix_pages_per_split = suf.pages_per_split;
   char* w = static_cast<char*>(workspace);
   a.pre_o = reinterpret_cast<float*>(w);
   w += align_up((size_t)a.prefix_chunks * rows * head_dim * 4, 256);
   a.pre_lse = reinterpret_cast<float*>(w);
   w += align_up((size_t)a.prefix_chunks * rows * 4, 256);
   a.suf_o = reinterpret_cast<float*>(w);
-  w += align_up(rows * head_dim * 4, 256);
+  w += align_up(rows * suf.num_splits * head_dim * 4, 256);
   a.suf_lse = reinterpret_cast<float*>(w);
   return launch_cascade(a, static_cast<cudaStream_t>(stream));
 }

@@ -100,6 +100,10 @@ bool decode_supported(int dtype, int head_dim, int page_size, int group) {
          page_size == 16 && (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
+int launch_decode_partials(const DecodeArgs& a, cudaStream_t stream) {
+  return a.unified ? dispatch_decode_unified(a, stream) : dispatch_decode<false>(a, stream);
+}
+
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int rc = a.unified ? dispatch_decode_unified(a, stream) : dispatch_decode<false>(a, stream);
   if (rc != PKV_OK) return rc;

@@ -159,20 +159,20 @@ decode_paged_kernel(const DecodeArgs a) {
   if (kv_len < 0 || kv_len > a.max_blocks * P) {
     if (split == 0) {
       if (threadIdx.x == 0) set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
-      write_group_const<T, D, G>(a, b, g, NAN, NAN);
+      if (!a.partial_only) write_group_const<T, D, G>(a, b, g, NAN, NAN);
     }
     return;
   }
   const int nblk = (kv_len + P - 1) / P;
   const int n_live = (nblk + a.pages_per_split - 1) / a.pages_per_split;
   if (n_live == 0) {
-    if (split == 0) write_group_const<T, D, G>(a, b, g, 0.0f, -INFINITY);
+    if (split == 0 && !a.partial_only) write_group_const<T, D, G>(a, b, g, 0.0f, -INFINITY);
     return;
   }
   if (split >= n_live) return;
   const int first = split * a.pages_per_split;
   const int n_pages = min(a.pages_per_split, nblk - first);
-  const bool final_write = (n_live == 1);
+  const bool final_write = (n_live == 1) && !a.partial_only;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + C::BAR_OFF;

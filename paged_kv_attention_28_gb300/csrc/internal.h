@@ -25,6 +25,9 @@ struct DecodeArgs {
   int num_splits, pages_per_split;
   float scale;
   int dtype;
+  // every live split writes an fp32 partial state, even a sequence's only split
+  // (used by the cascade path, whose own merge combines them with the prefix)
+  bool partial_only;
   // unified-max variant
   bool unified;
   float phi;
@@ -49,6 +52,8 @@ int decode_ctas_per_sm(int dtype, int head_dim, int group);
 
 // Enqueues the decode kernel (and the merge kernel when num_splits > 1).
 int launch_decode(const DecodeArgs& a, cudaStream_t stream);
+// Enqueues only the decode kernel (the caller merges the partial states).
+int launch_decode_partials(const DecodeArgs& a, cudaStream_t stream);
 bool decode_supported(int dtype, int head_dim, int page_size, int group);
 
 int launch_merge_pair(const float* out_a, const float* lse_a, const float* out_b,
@@ -84,11 +89,18 @@ struct CascadeArgs {
   // workspace carve-up
   float* pre_o;     // [prefix_chunks][n_requests][n_qo_heads][head_dim]
   float* pre_lse;   // [prefix_chunks][n_requests][n_qo_heads]
-  float* suf_o;     // [n_requests][n_qo_heads][head_dim]
-  float* suf_lse;   // [n_requests][n_qo_heads]
+  float* suf_o;     // [n_requests][n_qo_heads][suffix_splits][head_dim]
+  float* suf_lse;   // [n_requests][n_qo_heads][suffix_splits]
   int prefix_chunks;
+  int suffix_splits, suffix_pages_per_split;
 };
-int cascade_prefix_chunks(int prefix_len, int n_requests, int n_qo_heads, int n_kv_heads);
+// Chunks the shared prefix is cut into (0 when there is no prefix), from the shape
+// and the SM count of the current device.
+int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_qo_heads,
+                          int n_kv_heads);
+SplitPlan cascade_suffix_plan(int n_requests, int max_suffix_blocks, int n_qo_heads,
+                              int n_kv_heads, int head_dim, int dtype);
+int launch_cascade_prefix(const CascadeArgs& a, cudaStream_t stream);
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream);
 
 }  // namespace pkv
