@@ -12,86 +12,45 @@
 #include <cmath>
 
 #include "internal.h"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr float kLog2eC = 1.4426950408889634f;
 
-template <typename T>
-__device__ __forceinline__ T from_f32c(float x);
-template <>
-__device__ __forceinline__ float from_f32c<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32c<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+// One CTA per (request, query head) row: combines the prefix chunks' and the
+// suffix splits' partial states by log-sum-exp (merge_row_cta).
+constexpr int kCascadeMergeWarps = 8;
 
-// One warp per (request, query head) row: combines the prefix chunks' and the
-// suffix splits' partial states, M = max lse, w = exp(lse - M),
-// out = sum w O / sum w, lse = M + ln sum w.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) cascade_merge_kernel(const CascadeArgs a) {
-  constexpr int DL = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(const CascadeArgs a) {
+  const int row = blockIdx.x;
   const int rows = a.n_requests * a.n_qo_heads;
-  if (row >= rows) return;
   const int r = row / a.n_qo_heads;
   const int P = a.page_size;
   const int n_pre = a.prefix_len > 0 ? a.prefix_chunks : 0;
   const int L = __ldg(a.suffix_lens + r);
-  T* out = static_cast<T*>(a.out) + (size_t)row * D + lane * DL;
+  T* out = static_cast<T*>(a.out) + (size_t)row * D;
   if (L < 0 || L > a.max_suffix_blocks * P) {  // the decode kernel flagged it
-#pragma unroll
-    for (int e = 0; e < DL; ++e) out[e] = from_f32c<T>(NAN);
-    if (a.lse && lane == 0) a.lse[row] = NAN;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) out[d] = merge_cast<T>(NAN);
+    if (a.lse && threadIdx.x == 0) a.lse[row] = NAN;
     return;
   }
   const int nblk = (L + P - 1) / P;
   const int n_suf = (nblk + a.suffix_pages_per_split - 1) / a.suffix_pages_per_split;
-  // part i < n_pre: prefix chunk i; otherwise suffix split i - n_pre
-  auto part_lse = [&](int i) -> float {
-    return i < n_pre ? a.pre_lse[(size_t)i * rows + row]
-                     : a.suf_lse[(size_t)row * a.suffix_splits + (i - n_pre)];
-  };
-  auto part_o = [&](int i) -> const float* {
-    return i < n_pre ? a.pre_o + ((size_t)i * rows + row) * D
-                     : a.suf_o + ((size_t)row * a.suffix_splits + (i - n_pre)) * D;
-  };
-  const int n = n_pre + n_suf;
-  float M = -INFINITY;
-  for (int i = lane; i < n; i += 32) M = fmaxf(M, part_lse(i));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (n == 0 || M == -INFINITY) {
-#pragma unroll
-    for (int e = 0; e < DL; ++e) out[e] = from_f32c<T>(0.0f);
-    if (a.lse && lane == 0) a.lse[row] = -INFINITY;
-    return;
-  }
-  float acc[DL];
-#pragma unroll
-  for (int e = 0; e < DL; ++e) acc[e] = 0.0f;
-  float Ls = 0.0f;
-  for (int i = 0; i < n; ++i) {
-    const float w = ex2((part_lse(i) - M) * kLog2eC);
-    Ls += w;
-    const float* o = part_o(i) + lane * DL;
-    if constexpr (DL == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(o);
-      acc[0] = fmaf(w, x.x, acc[0]);
-      acc[1] = fmaf(w, x.y, acc[1]);
-      acc[2] = fmaf(w, x.z, acc[2]);
-      acc[3] = fmaf(w, x.w, acc[3]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, o[e], acc[e]);
-    }
-  }
-  const float inv = 1.0f / Ls;
-#pragma unroll
-  for (int e = 0; e < DL; ++e) out[e] = from_f32c<T>(acc[e] * inv);
-  if (a.lse && lane == 0) a.lse[row] = M + logf(Ls);
+  // partial i < n_pre: prefix chunk i; otherwise suffix split i - n_pre
+  merge_row_cta<T, D, kCascadeMergeWarps>(
+      n_pre + n_suf,
+      [&](int i) {
+        return i < n_pre ? a.pre_lse[(size_t)i * rows + row]
+                         : a.suf_lse[(size_t)row * a.suffix_splits + (i - n_pre)];
+      },
+      [&](int i) {
+        return i < n_pre ? a.pre_o + ((size_t)i * rows + row) * D
+                         : a.suf_o + ((size_t)row * a.suffix_splits + (i - n_pre)) * D;
+      },
+      out, a.lse ? a.lse + row : nullptr);
 }
 
 }  // namespace
@@ -117,8 +76,16 @@ int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_q
 
 SplitPlan cascade_suffix_plan(int n_requests, int max_suffix_blocks, int n_qo_heads,
                               int n_kv_heads, int head_dim, int dtype) {
-  return plan_decode_splits(n_requests, max_suffix_blocks, n_kv_heads, 0,
-                            decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads));
+  SplitPlan p = plan_decode_splits(n_requests, max_suffix_blocks, n_kv_heads, 0,
+                                   decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads));
+  // Suffix lengths vary widely from request to request, and the merge that follows
+  // takes the partial states anyway: cap a split at 16 pages so the CTAs stay short
+  // and the last wave stays full.
+  if (p.pages_per_split > 16) {
+    const int S = (max_suffix_blocks + 15) / 16;
+    p = plan_decode_splits(n_requests, max_suffix_blocks, n_kv_heads, S, 1);
+  }
+  return p;
 }
 
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream) {
@@ -155,9 +122,9 @@ int launch_cascade(const CascadeArgs& a, cudaStream_t stream) {
   const int rows = a.n_requests * a.n_qo_heads;
   if (a.head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (a.dtype == PKV_BF16)
-    cascade_merge_kernel<__nv_bfloat16, 128><<<(rows + 3) / 4, 128, 0, stream>>>(a);
+    cascade_merge_kernel<__nv_bfloat16, 128><<<rows, kCascadeMergeWarps * 32, 0, stream>>>(a);
   else
-    cascade_merge_kernel<float, 128><<<(rows + 3) / 4, 128, 0, stream>>>(a);
+    cascade_merge_kernel<float, 128><<<rows, kCascadeMergeWarps * 32, 0, stream>>>(a);
   return check_launch(cudaGetLastError());
 }
 

@@ -1,20 +1,17 @@
 // Online-softmax paged decode, the split merge, and the pairwise state merge.
 #include "decode_kernel.cuh"
+#include "merge.cuh"
 
 namespace pkv {
 
-// Combines the live splits of each (sequence, query head) row by log-sum-exp:
-// M = max_s lse_s, w_s = exp(lse_s - M), out = sum w_s O_s / sum w_s,
-// lse = M + ln sum w_s. FlashDecoding computes the partials independently and
-// updates them all at the end ("【FlashAttention-V4，非官方】FlashDecoding++",
-// section 1). Rows whose sequence fits in one split were written by the
-// decode kernel and are skipped here. One warp per row.
+// Combines the live splits of each (sequence, query head) row by log-sum-exp
+// (merge_row_cta). Rows whose sequence fits in one split were written by the
+// decode kernel and are skipped here. One CTA of eight warps per row.
+constexpr int kMergeWarps = 8;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) merge_splits_kernel(const DecodeArgs a) {
-  constexpr int DL = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row >= a.batch * a.n_qo_heads) return;
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_splits_kernel(const DecodeArgs a) {
+  const int row = blockIdx.x;
   const int b = row / a.n_qo_heads;
   const int P = a.page_size;
   const int L = __ldg(a.kv_lens + b);
@@ -24,39 +21,15 @@ __global__ void __launch_bounds__(128) merge_splits_kernel(const DecodeArgs a) {
   if (n_live < 2) return;
   const float* pl = a.part_lse + (size_t)row * a.num_splits;
   const float* po = a.part_o + (size_t)row * a.num_splits * D;
-  float M = -INFINITY;
-  for (int s = lane; s < n_live; s += 32) M = fmaxf(M, pl[s]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[DL];
-#pragma unroll
-  for (int e = 0; e < DL; ++e) acc[e] = 0.0f;
-  float Lsum = 0.0f;
-  for (int s = 0; s < n_live; ++s) {
-    const float w = ex2((pl[s] - M) * kLog2e);
-    Lsum += w;
-    float o[DL];
-    if constexpr (DL == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(po + (size_t)s * D + lane * 4);
-      o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(po + (size_t)s * D + lane * 2);
-      o[0] = x.x; o[1] = x.y;
-    }
-#pragma unroll
-    for (int e = 0; e < DL; ++e) acc[e] = fmaf(w, o[e], acc[e]);
-  }
-  const float inv = 1.0f / Lsum;
-  T* out = static_cast<T*>(a.out) + (size_t)row * D + lane * DL;
-#pragma unroll
-  for (int e = 0; e < DL; ++e) out[e] = from_f32<T>(acc[e] * inv);
-  if (a.lse && lane == 0) a.lse[row] = M + logf(Lsum);
+  merge_row_cta<T, D, kMergeWarps>(
+      n_live, [&](int i) { return pl[i]; }, [&](int i) { return po + (size_t)i * D; },
+      static_cast<T*>(a.out) + (size_t)row * D, a.lse ? a.lse + row : nullptr);
 }
 
 template <typename T, int D>
 int launch_merge_t(const DecodeArgs& a, cudaStream_t stream) {
   const int rows = a.batch * a.n_qo_heads;
-  merge_splits_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(a);
+  merge_splits_kernel<T, D><<<rows, kMergeWarps * 32, 0, stream>>>(a);
   return check_launch(cudaGetLastError());
 }
 
