@@ -48,14 +48,16 @@ constexpr int BN = 128;        // keys per tile
 constexpr int HD = 128;        // head dim
 constexpr int SUB = 16384;     // one 128-row x 64-column bf16 sub-tile (128-byte swizzle)
 constexpr int TILE = 2 * SUB;  // 128 x 128 bf16
-constexpr int NST = 2;         // K/V ring stages
+constexpr int NSK = 3;         // K ring stages (a K tile is free once both S products read it)
+constexpr int NSV = 2;         // V ring stages (a V tile is free once both PV products read it)
 constexpr int SM_Q = 0;                      // Q_A, Q_B
 constexpr int SM_K = SM_Q + 2 * TILE;
-constexpr int SM_V = SM_K + NST * TILE;
-constexpr int SM_BAR = SM_V + NST * TILE;
-// barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], o_done[2], drain
-constexpr int BAR_Q = 0, BAR_KVF = 1, BAR_KVE = 3, BAR_SF = 5, BAR_PF = 7, BAR_OD = 9,
-              BAR_DRAIN = 11, NBAR = 12;
+constexpr int SM_V = SM_K + NSK * TILE;
+constexpr int SM_BAR = SM_V + NSV * TILE;
+// barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
+// o_done[2], drain, q_empty (products of an item done with Q), o_free[2] (epilogue read O)
+constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 13,
+              BAR_OD = 15, BAR_DRAIN = 17, BAR_QE = 18, BAR_OF = 19, NBAR = 21;
 constexpr int SM_MISC = SM_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = SM_MISC + 64 + 1024;  // + slack to align the base to 1024
 constexpr int THREADS = 320;
@@ -134,7 +136,7 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 
 // Where a query tile's rows go and which keys its last tile may use.
 struct TileJob {
-  int n_tiles;     // key tiles this query tile walks
+  int n_tiles;     // key tiles this query tile walks (0: the tile does not exist)
   int last_valid;  // keys usable in its last key tile (prefix); unused when causal
   // causal: output rows t = q0 + r of (b, h)
   int q0, b, h;
@@ -142,139 +144,207 @@ struct TileJob {
   int r0, g, c;
 };
 
-// The softmax warpgroup of one query tile: S -> P for every key tile, then the epilogue.
+// One work item: two query tiles (A, B) that share their key tiles.
+struct Item {
+  TileJob A, B;
+  int n_kv;      // key tiles the item walks (B's count when B exists)
+  int kv_first;  // prefix: first key tile of the chunk
+  int hk;        // KV head
+  int qrow;      // causal: first query row of A; prefix: first (request, head) row of A
+  int b;         // causal: batch
+};
+
 template <bool CAUSAL>
-__device__ __forceinline__ void softmax_tile(const TileArgs& a, Misc* misc, uint32_t bar_sf,
-                                             uint32_t bar_pf, uint32_t bar_od, uint32_t col_s,
-                                             uint32_t col_o, const TileJob& job, int warp, int lane) {
+__device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
+  Item it{};
+  const int H = a.n_qo_heads;
+  const int G = a.n_qo_heads / a.n_kv_heads;
+  if constexpr (CAUSAL) {
+    const int n_qt = (a.seq_len + BM - 1) / BM;
+    const int n_pairs = (n_qt + 1) / 2;
+    // Longest first: the pairs nearest the end of the sequence have the most key tiles.
+    const int pr = n_pairs - 1 - id / (H * a.batch);
+    const int rem = id % (H * a.batch);
+    const int h = rem % H;
+    const int b = rem / H;
+    const int qtA = 2 * pr;
+    const bool has_b = (qtA + 1) < n_qt;
+    it.hk = h / G;
+    it.b = b;
+    it.n_kv = has_b ? qtA + 2 : qtA + 1;
+    it.qrow = qtA * BM;
+    it.A = TileJob{qtA + 1, BN, qtA * BM, b, h, 0, 0, 0};
+    it.B = TileJob{has_b ? qtA + 2 : 0, BN, (qtA + 1) * BM, b, h, 0, 0, 0};
+  } else {
+    const int c = id % a.n_chunks;
+    const int rest = id / a.n_chunks;
+    const int hk = rest % a.n_kv_heads;
+    const int pr = rest / a.n_kv_heads;
+    const int n_tiles = (a.n_prefix_pages + 7) / 8;
+    it.hk = hk;
+    it.kv_first = c * a.tiles_per_chunk;
+    it.n_kv = min(a.tiles_per_chunk, n_tiles - it.kv_first);
+    const bool has_b = (pr * 2 * BM + BM) < a.n_requests * G;
+    it.qrow = pr * 2 * BM;
+    const int last_valid = a.prefix_len - (it.kv_first + it.n_kv - 1) * BN;
+    it.A = TileJob{it.n_kv, last_valid, 0, 0, 0, it.qrow / G, hk, c};
+    it.B = TileJob{has_b ? it.n_kv : 0, last_valid, 0, 0, 0, (it.qrow + BM) / G, hk, c};
+  }
+  return it;
+}
+
+// The softmax warpgroup of one query tile of every item of this CTA: S -> P for each
+// key tile, then the epilogue. Phase counters run across items.
+template <bool CAUSAL>
+__device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint32_t bar_sf,
+                                             uint32_t bar_pf, uint32_t bar_od, uint32_t bar_of,
+                                             uint32_t col_s, uint32_t col_o, int tile, int n_items,
+                                             int warp, int lane) {
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;  // row in the tile = TMEM lane
   const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
   const uint32_t tS = misc->tmem_base + lane_addr + col_s;
   const uint32_t tO = misc->tmem_base + lane_addr + col_o;
   const float c = a.scale * kLog2eF;  // logits in log2 units: s * c
-  float ms = -INFINITY;               // reference max, log2 units
-  float l = 0.0f;
-  bool ok = true;
-  const int n_tiles = job.n_tiles;
-  for (int jj = 0; jj < n_tiles; ++jj) {
-    if (!warp_wait(bar_sf, jj & 1)) { ok = false; break; }
-    tc_fence_after();
-    uint32_t sr[128];
-    tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(sr + 0));
-    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 64));
-    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sr + 96));
-    tmem_ld_wait();
-    float* x = reinterpret_cast<float*>(sr);
-    if (jj == n_tiles - 1) {
-      // causal: key column i is visible to row r iff i <= r (diagonal tile);
-      // prefix: only the first last_valid keys of the last tile exist
-      const int limit = CAUSAL ? r + 1 : job.last_valid;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) x[i] = (i >= limit) ? -INFINITY : x[i];
-    }
-    float mx = fmaxf(x[0], x[1]);
-#pragma unroll
-    for (int i = 2; i < 128; i += 2) mx = max3(mx, x[i], x[i + 1]);
-    const float mt = mx * c;
-    const bool need = mt > ms + kRescaleSlack;  // always on the first tile (ms = -inf)
-    const float m_new = need ? mt : ms;
-    const float alpha = need ? ex2(ms - m_new) : 1.0f;
-    const uint64_t cc = f2(c, c);
-    const uint64_t mm = f2(-m_new, -m_new);
-    uint64_t acc = f2(0.0f, 0.0f);
-    uint32_t pk[64];
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      float y0, y1;
-      unf2(fma2(f2(x[2 * i], x[2 * i + 1]), cc, mm), y0, y1);
-      const float p0 = ex2(y0), p1 = ex2(y1);
-      acc = add2(acc, f2(p0, p1));
-      pk[i] = pack_bf16x2(p0, p1);
-    }
-    float s0, s1;
-    unf2(acc, s0, s1);
-    l = l * alpha + (s0 + s1);
-    // S_j's completion implies PV_{j-1} has completed (the commit for S_j was
-    // issued after it), so O is stable here and P's columns are free.
-    if (jj > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t o[32];
-        tmem_ld32(tO + q * 32, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO + q * 32, o);
-      }
-    }
-    ms = m_new;
-    tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(pk + 0));
-    tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(bar_pf);
-  }
-  // ------------------------------------------------------------------ epilogue
-  ok = __all_sync(0xffffffffu, ok);
-  if (ok && !warp_wait(bar_od, (n_tiles - 1) & 1)) ok = false;
-  tc_fence_after();
-  if (!ok && lane == 0) fail(misc, a.err_flag);
-  if (*reinterpret_cast<volatile int*>(&misc->bad_page)) ok = false;
-  const float inv = ok ? 1.0f / l : NAN;
-  const float lse_row = ok ? (ms + log2f(l)) * kLn2F : NAN;
   const int H = a.n_qo_heads;
-  if constexpr (CAUSAL) {
-    const int t = job.q0 + r;
-    const bool store = t < a.seq_len;  // rows past a ragged end are computed but not stored
-    __nv_bfloat16* orow =
-        static_cast<__nv_bfloat16*>(a.out) + (((size_t)job.b * a.seq_len + t) * H + job.h) * HD;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t o[32];
-      tmem_ld32(tO + q * 32, o);  // all lanes, uniformly
+  uint32_t sf_cnt = 0, od_cnt = 0;
+  bool ok = true;
+  for (int id = blockIdx.x; id < n_items; id += gridDim.x) {
+    const Item it = make_item<CAUSAL>(a, id);
+    const TileJob& job = tile == 0 ? it.A : it.B;
+    const int n_tiles = job.n_tiles;
+    if (n_tiles == 0) continue;
+    float ms = -INFINITY;  // reference max, log2 units
+    float l = 0.0f;
+    for (int jj = 0; jj < n_tiles; ++jj) {
+      if (ok && !warp_wait(bar_sf, sf_cnt & 1)) ok = false;
+      ++sf_cnt;
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(sr + 0));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 64));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sr + 96));
       tmem_ld_wait();
-      uint4 w[4];
-      uint32_t* wp = reinterpret_cast<uint32_t*>(w);
+      float* x = reinterpret_cast<float*>(sr);
+      if (jj == n_tiles - 1) {
+        // causal: key column i is visible to row r iff i <= r (diagonal tile);
+        // prefix: only the first last_valid keys of the last tile exist
+        const int limit = CAUSAL ? r + 1 : job.last_valid;
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        wp[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = w[i];
+        for (int i = 0; i < 128; ++i) x[i] = (i >= limit) ? -INFINITY : x[i];
       }
+      // row max over four independent chains
+      float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]), m2 = fmaxf(x[4], x[5]),
+            m3 = fmaxf(x[6], x[7]);
+#pragma unroll
+      for (int i = 8; i < 128; i += 8) {
+        m0 = max3(m0, x[i], x[i + 1]);
+        m1 = max3(m1, x[i + 2], x[i + 3]);
+        m2 = max3(m2, x[i + 4], x[i + 5]);
+        m3 = max3(m3, x[i + 6], x[i + 7]);
+      }
+      const float mt = max3(m0, m1, fmaxf(m2, m3)) * c;
+      const bool need = mt > ms + kRescaleSlack;  // always on the first tile (ms = -inf)
+      const float m_new = need ? mt : ms;
+      const float alpha = need ? ex2(ms - m_new) : 1.0f;
+      const uint64_t cc = f2(c, c);
+      const uint64_t mm = f2(-m_new, -m_new);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      // P in two halves of 32 packed columns; the S values are all in registers
+      // already, so P may overwrite the start of its own S buffer right away.
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = hlf * 64 + 2 * i;
+          float y0, y1;
+          unf2(fma2(f2(x[e], x[e + 1]), cc, mm), y0, y1);
+          const float p0 = ex2(y0), p1 = ex2(y1);
+          acc[i & 3] = add2(acc[i & 3], f2(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + hlf * 32, pk);
+      }
+      float s0, s1, s2, s3, s4, s5, s6, s7;
+      unf2(acc[0], s0, s1);
+      unf2(acc[1], s2, s3);
+      unf2(acc[2], s4, s5);
+      unf2(acc[3], s6, s7);
+      l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
+      // S_j's completion implies PV_{j-1} has completed (the commit for S_j was
+      // issued after it), so O is stable here and P's columns are free.
+      if (jj > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + q * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + q * 32, o);
+        }
+      }
+      ms = m_new;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_pf);
     }
-    if (store && a.lse) a.lse[((size_t)job.b * H + job.h) * a.seq_len + t] = lse_row;
-  } else {
-    const int G = a.n_qo_heads / a.n_kv_heads;
-    const int req = job.r0 + r / G;
-    const int h = job.g * G + r % G;
-    const bool store = req < a.n_requests;
-    const size_t row = ((size_t)job.c * a.n_requests + req) * H + h;
-    float* orow = a.part_o + row * HD;
+    // ---------------------------------------------------------------- epilogue
+    od_cnt += n_tiles;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !warp_wait(bar_od, (od_cnt - 1) & 1)) ok = false;
+    tc_fence_after();
+    if (!ok && lane == 0) fail(misc, a.err_flag);
+    if (*reinterpret_cast<volatile int*>(&misc->bad_page)) ok = false;
+    uint32_t o[128];
+    tmem_ld32(tO + 0, *reinterpret_cast<uint32_t(*)[32]>(o + 0));
+    tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+    tmem_ld32(tO + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
+    tmem_ld32(tO + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
+    tmem_ld_wait();
+    // O is in registers: the next item's first PV may overwrite it.
+    tc_fence_before();
+    mbar_arrive(bar_of);
+    const float inv = ok ? 1.0f / l : NAN;
+    const float lse_row = ok ? (ms + log2f(l)) * kLn2F : NAN;
+    if constexpr (CAUSAL) {
+      const int t = job.q0 + r;
+      if (t < a.seq_len) {  // rows past a ragged end are computed but not stored
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                              (((size_t)job.b * a.seq_len + t) * H + job.h) * HD);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t o[32];
-      tmem_ld32(tO + q * 32, o);
-      tmem_ld_wait();
-      if (store) {
-        float4* dst = reinterpret_cast<float4*>(orow + q * 32);
+        for (int i = 0; i < 16; ++i)
+          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
+                              pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
+                              pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
+                              pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
+        if (a.lse) a.lse[((size_t)job.b * H + job.h) * a.seq_len + t] = lse_row;
+      }
+    } else {
+      const int G = a.n_qo_heads / a.n_kv_heads;
+      const int req = job.r0 + r / G;
+      if (req < a.n_requests) {
+        const int h = job.g * G + r % G;
+        const size_t row = ((size_t)job.c * a.n_requests + req) * H + h;
+        float4* dst = reinterpret_cast<float4*>(a.part_o + row * HD);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 32; ++i)
           dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        a.part_lse[row] = lse_row;
       }
     }
-    if (store) a.part_lse[row] = lse_row;
   }
 }
 
+// Persistent: one CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x, ...
 template <bool CAUSAL>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                 const __grid_constant__ CUtensorMap mv, const TileArgs a) {
+                 const __grid_constant__ CUtensorMap mv, const TileArgs a, int n_items) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -285,52 +355,13 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int H = a.n_qo_heads;
   const int G = a.n_qo_heads / a.n_kv_heads;
-  const int id = blockIdx.x;
-
-  // ---------------------------------------------------------------- what this CTA does
-  TileJob jobA{}, jobB{};
-  bool has_b;
-  int n_kv;      // key tiles the CTA walks
-  int lastA;     // A's last key tile
-  int kv_first;  // prefix: first key tile of the chunk
-  int hk, qrow;  // KV head; causal: first query row of A
-  if constexpr (CAUSAL) {
-    const int n_qt = (a.seq_len + BM - 1) / BM;
-    const int n_pairs = (n_qt + 1) / 2;
-    // Longest-first order: the pairs nearest the end of the sequence have the most key tiles.
-    const int pr = n_pairs - 1 - id / (H * a.batch);
-    const int rem = id % (H * a.batch);
-    const int h = rem % H;
-    const int b = rem / H;
-    hk = h / G;
-    const int qtA = 2 * pr;
-    has_b = (qtA + 1) < n_qt;
-    lastA = qtA;
-    n_kv = has_b ? qtA + 2 : qtA + 1;
-    kv_first = 0;
-    qrow = qtA * BM;
-    jobA = TileJob{qtA + 1, BN, qtA * BM, b, h, 0, 0, 0};
-    jobB = TileJob{qtA + 2, BN, (qtA + 1) * BM, b, h, 0, 0, 0};
-  } else {
-    const int c = id % a.n_chunks;
-    const int rest = id / a.n_chunks;
-    hk = rest % a.n_kv_heads;
-    const int pr = rest / a.n_kv_heads;
-    const int n_tiles = (a.n_prefix_pages + 7) / 8;
-    kv_first = c * a.tiles_per_chunk;
-    n_kv = min(a.tiles_per_chunk, n_tiles - kv_first);
-    lastA = n_kv - 1;
-    has_b = (pr * 2 * BM + BM) < a.n_requests * G;
-    qrow = pr * 2 * BM;  // row of the (request, head-in-group) list
-    const int last_valid = a.prefix_len - (kv_first + n_kv - 1) * BN;
-    jobA = TileJob{n_kv, last_valid, 0, 0, 0, qrow / G, hk, c};
-    jobB = TileJob{n_kv, last_valid, 0, 0, 0, (qrow + BM) / G, hk, c};
-  }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == BAR_PF || i == BAR_PF + 1) ? 128 : 1);
+    for (int i = 0; i < NBAR; ++i) {
+      const bool per_thread = (i == BAR_PF || i == BAR_PF + 1 || i == BAR_OF || i == BAR_OF + 1);
+      mbar_init(bar(i), per_thread ? 128 : 1);
+    }
     misc->abort_ = 0;
     misc->bad_page = 0;
     fence_mbar_init();
@@ -350,108 +381,165 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       tma_prefetch_desc(&mq);
       tma_prefetch_desc(&mk);
       tma_prefetch_desc(&mv);
-      mbar_arrive_expect_tx(bar(BAR_Q), 2 * TILE);
-      for (int t = 0; t < 2; ++t) {
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
-          if constexpr (CAUSAL)
-            tma_load_4d(dst, &mq, half * 64, jobA.h, qrow + t * BM, jobA.b, bar(BAR_Q));
-          else
-            tma_load_3d(dst, &mq, half * 64, hk * G, (qrow + t * BM) / G, bar(BAR_Q));
-        }
-      }
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NST, u = j / NST;
-        if (u > 0 && !mbar_wait(bar(BAR_KVE + s), (u - 1) & 1)) {
-          fail(misc, a.err_flag);
-          break;
-        }
-        if (misc->abort_) break;
-        mbar_arrive_expect_tx(bar(BAR_KVF + s), 2 * TILE);
-        const uint32_t dk = sb + SM_K + s * TILE, dv = sb + SM_V + s * TILE;
+      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
+      bool ok = true;
+      // One 128-key tile of K or V (32 KiB) into its ring.
+      auto load_tile = [&](const Item& it, int j, bool is_v) -> bool {
+        uint32_t& cnt = is_v ? v_cnt : k_cnt;
+        const uint32_t ns = is_v ? NSV : NSK;
+        const uint32_t s = cnt % ns, u = cnt / ns;
+        const uint32_t full = bar((is_v ? BAR_VF : BAR_KF) + s);
+        if (u > 0 && !mbar_wait(bar((is_v ? BAR_VE : BAR_KE) + s), (u - 1) & 1)) return false;
+        if (misc->abort_) return false;
+        mbar_arrive_expect_tx(full, TILE);
+        const uint32_t dst = sb + (is_v ? SM_V : SM_K) + s * TILE;
+        const CUtensorMap* map = is_v ? &mv : &mk;
         if constexpr (CAUSAL) {
           const int k0 = j * BN;
-          tma_load_4d(dk, &mk, 0, hk, k0, jobA.b, bar(BAR_KVF + s));
-          tma_load_4d(dk + SUB, &mk, 64, hk, k0, jobA.b, bar(BAR_KVF + s));
-          tma_load_4d(dv, &mv, 0, hk, k0, jobA.b, bar(BAR_KVF + s));
-          tma_load_4d(dv + SUB, &mv, 64, hk, k0, jobA.b, bar(BAR_KVF + s));
+          tma_load_4d(dst, map, 0, it.hk, k0, it.b, full);
+          tma_load_4d(dst + SUB, map, 64, it.hk, k0, it.b, full);
         } else {
           // Eight pages of 16 keys make one 128-key tile; each page is a 16-row box.
           // Slots past the prefix reload its first page (finite data; masked out).
           for (int pp = 0; pp < 8; ++pp) {
-            const int page_idx = (kv_first + j) * 8 + pp;
+            const int page_idx = (it.kv_first + j) * 8 + pp;
             int phys = __ldg(a.prefix_table + (page_idx < a.n_prefix_pages ? page_idx : 0));
             if (phys < 0 || phys >= a.num_pages) {
               misc->bad_page = 1;
               set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
               phys = 0;
             }
-            const int row = (phys * a.n_kv_heads + hk) * 16;
-            tma_load_2d(dk + pp * 2048, &mk, 0, row, bar(BAR_KVF + s));
-            tma_load_2d(dk + SUB + pp * 2048, &mk, 64, row, bar(BAR_KVF + s));
-            tma_load_2d(dv + pp * 2048, &mv, 0, row, bar(BAR_KVF + s));
-            tma_load_2d(dv + SUB + pp * 2048, &mv, 64, row, bar(BAR_KVF + s));
+            const int row = (phys * a.n_kv_heads + it.hk) * 16;
+            tma_load_2d(dst + pp * 2048, map, 0, row, full);
+            tma_load_2d(dst + SUB + pp * 2048, map, 64, row, full);
           }
         }
-        issued = j + 1;
+        ++cnt;
+        return true;
+      };
+      for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
+        const Item it = make_item<CAUSAL>(a, id);
+        // The item's first K tile goes out before its Q, which must wait until the
+        // previous item's products are done with the Q buffer. K then runs one tile
+        // ahead of V: K0, Q, K1, V0, K2, V1, ...
+        if (!load_tile(it, 0, false)) { ok = false; break; }
+        if (q_cnt > 0 && !mbar_wait(bar(BAR_QE), (q_cnt - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(BAR_Q), 2 * TILE);
+        for (int t = 0; t < 2; ++t) {
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
+            if constexpr (CAUSAL)
+              tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, bar(BAR_Q));
+            else
+              tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, bar(BAR_Q));
+          }
+        }
+        ++q_cnt;
+        for (int j = 0; ok && j < it.n_kv; ++j) {
+          if (j + 1 < it.n_kv && !load_tile(it, j + 1, false)) ok = false;
+          if (ok && !load_tile(it, j, true)) ok = false;
+        }
       }
+      if (!ok) fail(misc, a.err_flag);
       // Every issued copy must land before the CTA's shared memory is released
       // (immediate on the normal path, where the MMA warp already waited for them).
-      if (!mbar_wait(bar(BAR_Q), 0)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
-      for (int s = 0; s < NST && s < issued; ++s)
-        if (!mbar_wait(bar(BAR_KVF + s), ((issued - 1 - s) / NST) & 1))
-          set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      if (q_cnt > 0 && !mbar_wait(bar(BAR_Q), (q_cnt - 1) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      for (uint32_t s = 0; s < NSK && s < k_cnt; ++s)
+        if (!mbar_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      for (uint32_t s = 0; s < NSV && s < v_cnt; ++s)
+        if (!mbar_wait(bar(BAR_VF + s), ((v_cnt - 1 - s) / NSV) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
       const uint32_t idPV = idesc_bf16_f32(BM, HD, false, true);
-      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
-        const uint32_t kb = sb + SM_K + (j % NST) * TILE;
-        const uint32_t qb = sb + SM_Q + t * TILE;
+      // Descriptors are built once; a K step inside a tile only moves the start
+      // address, i.e. adds (byte offset >> 4) to the low field. The largest start
+      // (under 232 KB) plus the largest step stays inside the 14-bit field.
+      // Ring slots and the two Q tiles are TILE bytes apart, so a slot's descriptor is
+      // the first slot's plus slot * (TILE >> 4).
+      const uint64_t dq0 = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B);
+      const uint64_t dk0 = smem_desc(sb + SM_K, 16, 1024, kSwizzle128B);
+      const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
+      constexpr uint64_t kSlot = TILE >> 4;
+      auto issue_s = [&](int t, uint32_t kg) {  // S_t = Q_t K^T, K at ring position kg
+        const uint64_t a0 = dq0 + (uint64_t)t * kSlot, b0 = dk0 + (uint64_t)(kg % NSK) * kSlot;
+        const uint32_t d = tmem + COL_S + t * BN;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k / 4) * SUB + (k % 4) * 32;
-          mma_bf16_ss(tmem + COL_S + t * BN, smem_desc(qb + off, 16, 1024, kSwizzle128B),
-                      smem_desc(kb + off, 16, 1024, kSwizzle128B), idS, k > 0);
+          const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
+          mma_bf16_ss(d, a0 + off, b0 + off, idS, k > 0);
         }
         mma_commit(bar(BAR_SF + t));
       };
-      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j
-        const uint32_t vb = sb + SM_V + (j % NST) * TILE;
+      auto issue_pv = [&](int t, uint32_t vg, bool first) {  // O_t (+)= P_t V, V at ring position vg
+        const uint64_t b0 = dv0 + (uint64_t)(vg % NSV) * kSlot;
+        const uint32_t d = tmem + COL_O + t * HD, pa = tmem + COL_S + t * BN;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_bf16_ts(tmem + COL_O + t * HD, tmem + COL_S + t * BN + k * 8,
-                      smem_desc(vb + k * 2048, 16384, 1024, kSwizzle128B), idPV,
-                      (j > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(d, pa + k * 8, b0 + (uint64_t)((k * 2048) >> 4), idPV, (!first || k > 0) ? 1u : 0u);
         mma_commit(bar(BAR_OD + t));
       };
-      bool ok = mbar_wait(bar(BAR_Q), 0) && mbar_wait(bar(BAR_KVF + 0), 0);
-      if (ok) {
+      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, pf_cnt[2] = {0, 0}, of_cnt[2] = {0, 0},
+               of_need[2] = {0, 0};
+      bool ok = true;
+      auto wait_k = [&](uint32_t kg) { return mbar_wait(bar(BAR_KF + kg % NSK), (kg / NSK) & 1); };
+      auto wait_v = [&](uint32_t vg) { return mbar_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1); };
+      for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
+        const Item it = make_item<CAUSAL>(a, id);
+        const bool has_b = it.B.n_tiles > 0;
+        const int lastA = it.A.n_tiles - 1;
+        const int n_kv = it.n_kv;
+        if (!mbar_wait(bar(BAR_Q), q_cnt & 1) || !wait_k(k_cnt)) { ok = false; break; }
+        ++q_cnt;
         tc_fence_after();
-        issue_s(0, 0);
-        if (has_b) issue_s(1, 0);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j <= lastA) {
-          if (!mbar_wait(bar(BAR_PF + 0), j & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(0, j);
+        issue_s(0, k_cnt);
+        if (has_b) issue_s(1, k_cnt);
+        mma_commit(bar(BAR_KE + k_cnt % NSK));  // K_0 is read by no later product
+        for (int j = 0; j < n_kv; ++j) {
+          const uint32_t kg = k_cnt + j, vg = v_cnt + j;
+          bool v_ready = false;
+          if (j <= lastA) {
+            if (!mbar_wait(bar(BAR_PF + 0), pf_cnt[0] & 1)) { ok = false; break; }
+            ++pf_cnt[0];
+            // the previous item's epilogue must have read O_A before it is overwritten
+            if (j == 0 && of_need[0] > of_cnt[0]) {
+              if (!mbar_wait(bar(BAR_OF + 0), of_cnt[0] & 1)) { ok = false; break; }
+              ++of_cnt[0];
+            }
+            if (!wait_v(vg)) { ok = false; break; }
+            v_ready = true;
+            tc_fence_after();
+            issue_pv(0, vg, j == 0);
+          }
+          if (j + 1 < n_kv) {
+            if (!wait_k(kg + 1)) { ok = false; break; }
+            tc_fence_after();
+            if (j + 1 <= lastA) issue_s(0, kg + 1);
+          }
+          if (has_b) {
+            if (!mbar_wait(bar(BAR_PF + 1), pf_cnt[1] & 1)) { ok = false; break; }
+            ++pf_cnt[1];
+            if (j == 0 && of_need[1] > of_cnt[1]) {
+              if (!mbar_wait(bar(BAR_OF + 1), of_cnt[1] & 1)) { ok = false; break; }
+              ++of_cnt[1];
+            }
+            if (!v_ready && !wait_v(vg)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(1, vg, j == 0);
+          }
+          mma_commit(bar(BAR_VE + vg % NSV));  // V_j is read by no later product
+          if (j + 1 < n_kv) {
+            if (has_b) issue_s(1, kg + 1);
+            mma_commit(bar(BAR_KE + (kg + 1) % NSK));  // nor is K_{j+1}
+          }
         }
-        if (j + 1 < n_kv) {
-          if (!mbar_wait(bar(BAR_KVF + (j + 1) % NST), ((j + 1) / NST) & 1)) { ok = false; break; }
-          tc_fence_after();
-          if (j + 1 <= lastA) issue_s(0, j + 1);
-        }
-        if (has_b) {
-          if (!mbar_wait(bar(BAR_PF + 1), j & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(1, j);
-        }
-        mma_commit(bar(BAR_KVE + j % NST));  // K_j / V_j are no longer read by any product
-        if (has_b && j + 1 < n_kv) issue_s(1, j + 1);
+        mma_commit(bar(BAR_QE));  // every product that reads Q of this item has been issued
+        k_cnt += n_kv;
+        v_cnt += n_kv;
+        ++of_need[0];
+        if (has_b) ++of_need[1];
       }
       if (!ok) fail(misc, a.err_flag);
       // Every issued product must finish before TMEM is freed.
@@ -459,11 +547,11 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       if (!mbar_wait(bar(BAR_DRAIN), 0)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp < 6) {
-    softmax_tile<CAUSAL>(a, misc, bar(BAR_SF + 0), bar(BAR_PF + 0), bar(BAR_OD + 0), COL_S, COL_O,
-                         jobA, warp, lane);
-  } else if (has_b) {
-    softmax_tile<CAUSAL>(a, misc, bar(BAR_SF + 1), bar(BAR_PF + 1), bar(BAR_OD + 1), COL_S + BN,
-                         COL_O + HD, jobB, warp, lane);
+    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + 0), bar(BAR_PF + 0), bar(BAR_OD + 0), bar(BAR_OF + 0),
+                         COL_S, COL_O, 0, n_items, warp, lane);
+  } else {
+    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + 1), bar(BAR_PF + 1), bar(BAR_OD + 1), bar(BAR_OF + 1),
+                         COL_S + BN, COL_O + HD, 1, n_items, warp, lane);
   }
 
   tc_fence_before();
@@ -507,9 +595,9 @@ bool make_btHd_map(CUtensorMap* m, const void* ptr, int B, int T, int H) {
 
 template <bool CAUSAL>
 int launch_tiles(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                 const TileArgs& a, long grid, cudaStream_t stream) {
-  if (grid <= 0) return PKV_OK;
-  if (grid > 0x7fffffffL) return PKV_ERR_UNSUPPORTED;
+                 const TileArgs& a, long n_items, cudaStream_t stream) {
+  if (n_items <= 0) return PKV_OK;
+  if (n_items > 0x7fffffffL) return PKV_ERR_UNSUPPORTED;
   static int configured_mask = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -519,7 +607,10 @@ int launch_tiles(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap
       return PKV_ERR_LAUNCH;
     configured_mask |= (1 << dev);
   }
-  attn_tile_kernel<CAUSAL><<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, a);
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 1;
+  const long grid = n_items < sms ? n_items : sms;  // one persistent CTA per SM
+  attn_tile_kernel<CAUSAL><<<(unsigned)grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, a, (int)n_items);
   return check_launch(cudaGetLastError());
 }
 
