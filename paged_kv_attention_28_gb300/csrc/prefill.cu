@@ -12,11 +12,15 @@
 // alternates with the tensor core: while one warpgroup turns S_A into P_A, the
 // tensor core runs B's products, and the other way round.
 //
-// Warp roles (320 threads):
-//   warp 0     TMA producer (Q_A and Q_B once, K/V tiles into a 2-stage ring); owns TMEM
-//   warp 1     MMA issuer (one thread)
-//   warps 2-5  softmax of tile A, one thread per row (warp w reads TMEM lanes 32*(w%4)..)
-//   warps 6-9  softmax of tile B
+// Warp roles (512 threads, four warpgroups):
+//   warpgroup 0: warp 0 TMA producer (Q_A and Q_B per item, K tiles into a 3-stage ring,
+//                V tiles into a 2-stage ring; owns TMEM), warps 1 and 2 MMA issuers of
+//                tiles A and B (one thread each), warp 3 idle
+//   warpgroup 1: softmax of tile A, one thread per row (warp w reads TMEM lanes 32*(w%4)..)
+//   warpgroup 2: softmax of tile B
+//   warpgroup 3: epilogue: O / l out of TMEM to global memory, for both tiles
+// Registers are rebalanced with setmaxnreg: the softmax warpgroups get 168 per thread,
+// the other two 88 (88 + 168 + 168 + 88 = 512 per SM sub-partition, the launch's share).
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // P overwrites the first 64 columns of its own S buffer (packed bf16 pairs).
 // PV reads A = P from TMEM and B = V (MN-major) from shared memory.
@@ -54,13 +58,20 @@ constexpr int SM_Q = 0;                      // Q_A, Q_B
 constexpr int SM_K = SM_Q + 2 * TILE;
 constexpr int SM_V = SM_K + NSK * TILE;
 constexpr int SM_BAR = SM_V + NSV * TILE;
-// barriers: q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
-// o_done[2], drain, q_empty (products of an item done with Q), o_free[2] (epilogue read O)
+// barriers: q_full[2], k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
+// o_done[2], drain[2], q_empty[2] (products of an item done with a Q tile), o_free[2]
+// (epilogue read O). k_empty and v_empty take one arrival from each MMA issuer.
 constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 13,
-              BAR_OD = 15, BAR_DRAIN = 17, BAR_QE = 18, BAR_OF = 19, NBAR = 21;
-constexpr int SM_MISC = SM_BAR + NBAR * 8;
+              BAR_OD = 15, BAR_DRAIN = 17, BAR_QE = 19, BAR_OF = 21, BAR_Q1 = 23, BAR_ST = 24, BAR_IE = 26,
+              NBAR = 28;
+// q_full and q_empty exist per query tile: tile t's Q uses BAR_Q / BAR_Q1 and BAR_QE + t.
+// st_full[2]: a tile's softmax has written its rows' 1/l for the epilogue warpgroup;
+// inv_empty[2]: the epilogue has read them, so the next item's softmax may overwrite them.
+constexpr int SM_INV = SM_BAR + NBAR * 8;          // float [2 tiles][128 rows]: 1/l per row
+constexpr int SM_MISC = SM_INV + 2 * BM * 4;
 constexpr int SMEM_BYTES = SM_MISC + 64 + 1024;  // + slack to align the base to 1024
-constexpr int THREADS = 320;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+constexpr int THREADS = 512;  // four warpgroups; see the role list at the top
 constexpr int TMEM_COLS = 512;
 constexpr int COL_S = 0, COL_O = 256;
 constexpr float kLog2eF = 1.4426950408889634f;
@@ -197,7 +208,8 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
 // key tile, then the epilogue. Phase counters run across items.
 template <bool CAUSAL>
 __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint32_t bar_sf,
-                                             uint32_t bar_pf, uint32_t bar_od, uint32_t bar_of,
+                                             uint32_t bar_pf, uint32_t bar_st, uint32_t bar_ie,
+                                             float* inv_rows,
                                              uint32_t col_s, uint32_t col_o, int tile, int n_items,
                                              int warp, int lane) {
   const int quarter = warp & 3;
@@ -207,7 +219,7 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
   const uint32_t tO = misc->tmem_base + lane_addr + col_o;
   const float c = a.scale * kLog2eF;  // logits in log2 units: s * c
   const int H = a.n_qo_heads;
-  uint32_t sf_cnt = 0, od_cnt = 0;
+  uint32_t sf_cnt = 0, st_cnt = 0;
   bool ok = true;
   for (int id = blockIdx.x; id < n_items; id += gridDim.x) {
     const Item it = make_item<CAUSAL>(a, id);
@@ -292,49 +304,103 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
       tc_fence_before();
       mbar_arrive(bar_pf);
     }
-    // ---------------------------------------------------------------- epilogue
-    od_cnt += n_tiles;
+    // ---------------------------------------------------------------- hand-off
+    // The row's LSE goes out here; 1/l goes to the epilogue warpgroup, which
+    // divides O once the item's last PV is done.
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && !warp_wait(bar_od, (od_cnt - 1) & 1)) ok = false;
-    tc_fence_after();
     if (!ok && lane == 0) fail(misc, a.err_flag);
     if (*reinterpret_cast<volatile int*>(&misc->bad_page)) ok = false;
-    uint32_t o[128];
-    tmem_ld32(tO + 0, *reinterpret_cast<uint32_t(*)[32]>(o + 0));
-    tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
-    tmem_ld32(tO + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
-    tmem_ld32(tO + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
-    tmem_ld_wait();
-    // O is in registers: the next item's first PV may overwrite it.
-    tc_fence_before();
-    mbar_arrive(bar_of);
-    const float inv = ok ? 1.0f / l : NAN;
     const float lse_row = ok ? (ms + log2f(l)) * kLn2F : NAN;
     if constexpr (CAUSAL) {
       const int t = job.q0 + r;
-      if (t < a.seq_len) {  // rows past a ragged end are computed but not stored
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                              (((size_t)job.b * a.seq_len + t) * H + job.h) * HD);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
-                              pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
-                              pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
-                              pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
-        if (a.lse) a.lse[((size_t)job.b * H + job.h) * a.seq_len + t] = lse_row;
-      }
+      if (t < a.seq_len && a.lse) a.lse[((size_t)job.b * H + job.h) * a.seq_len + t] = lse_row;
     } else {
       const int G = a.n_qo_heads / a.n_kv_heads;
       const int req = job.r0 + r / G;
-      if (req < a.n_requests) {
-        const int h = job.g * G + r % G;
-        const size_t row = ((size_t)job.c * a.n_requests + req) * H + h;
+      if (req < a.n_requests)
+        a.part_lse[((size_t)job.c * a.n_requests + req) * H + job.g * G + r % G] = lse_row;
+    }
+    if (st_cnt > 0 && ok && !warp_wait(bar_ie, (st_cnt - 1) & 1)) ok = false;
+    inv_rows[r] = ok ? 1.0f / l : NAN;
+    ++st_cnt;
+    mbar_arrive(bar_st);
+  }
+}
+
+// The epilogue warpgroup: for each item and each of its query tiles, waits for the
+// tile's 1/l and its last PV, then writes O / l to global memory and frees O.
+template <bool CAUSAL>
+__device__ __forceinline__ void epilogue_loop(const TileArgs& a, Misc* misc, uint32_t (&bars)[8],
+                                              const float* inv_rows_base, int n_items, int warp,
+                                              int lane) {
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;
+  const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
+  const int H = a.n_qo_heads;
+  uint32_t st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
+  bool ok = true;
+  for (int id = blockIdx.x; id < n_items; id += gridDim.x) {
+    const Item it = make_item<CAUSAL>(a, id);
+    for (int t = 0; t < 2; ++t) {
+      const TileJob& job = t == 0 ? it.A : it.B;
+      if (job.n_tiles == 0) continue;
+      const uint32_t bar_st = bars[t], bar_od = bars[2 + t], bar_of = bars[4 + t], bar_ie = bars[6 + t];
+      od_cnt[t] += job.n_tiles;
+      // The softmax finished the item's last tile, so at most its last PV is pending.
+      if (ok && !warp_wait(bar_st, st_cnt[t] & 1)) ok = false;
+      ++st_cnt[t];
+      if (ok && !warp_wait(bar_od, (od_cnt[t] - 1) & 1)) ok = false;
+      tc_fence_after();
+      if (!ok && lane == 0) fail(misc, a.err_flag);
+      const float inv = ok ? inv_rows_base[t * BM + r] : NAN;
+      mbar_arrive(bar_ie);  // the softmax may write this tile's next 1/l
+      const uint32_t tO = misc->tmem_base + lane_addr + COL_O + t * HD;
+      if constexpr (CAUSAL) {
+        const int tt = job.q0 + r;
+        const bool store = tt < a.seq_len;  // rows past a ragged end are computed but not stored
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                              (((size_t)job.b * a.seq_len + tt) * H + job.h) * HD);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + q * 32, o);
+          tmem_ld_wait();
+          if (q == 3) {  // O is out of TMEM: the next item's first PV may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar_of);
+          }
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[q * 4 + i] = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
+                  pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
+                  pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
+                  pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
+          }
+        }
+      } else {
+        const int G = a.n_qo_heads / a.n_kv_heads;
+        const int req = job.r0 + r / G;
+        const bool store = req < a.n_requests;
+        const size_t row = ((size_t)job.c * a.n_requests + (store ? req : 0)) * H + job.g * G + r % G;
         float4* dst = reinterpret_cast<float4*>(a.part_o + row * HD);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                               __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
-        a.part_lse[row] = lse_row;
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + q * 32, o);
+          tmem_ld_wait();
+          if (q == 3) {
+            tc_fence_before();
+            mbar_arrive(bar_of);
+          }
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[q * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                           __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+          }
+        }
       }
     }
   }
@@ -359,8 +425,10 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
-      const bool per_thread = (i == BAR_PF || i == BAR_PF + 1 || i == BAR_OF || i == BAR_OF + 1);
-      mbar_init(bar(i), per_thread ? 128 : 1);
+      const bool per_thread = (i == BAR_PF || i == BAR_PF + 1 || i == BAR_OF || i == BAR_OF + 1 ||
+                               i == BAR_ST || i == BAR_ST + 1 || i == BAR_IE || i == BAR_IE + 1);
+      const bool per_issuer = (i >= BAR_KE && i < BAR_KE + NSK) || (i >= BAR_VE && i < BAR_VE + NSV);
+      mbar_init(bar(i), per_thread ? 128 : (per_issuer ? 2 : 1));
     }
     misc->abort_ = 0;
     misc->bad_page = 0;
@@ -374,7 +442,9 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-
+  // Registers are rebalanced between warpgroups at the head of each role (setmaxnreg is
+  // warpgroup-wide: every warp of a warpgroup executes the same one).
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -419,139 +489,152 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       };
       for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
         const Item it = make_item<CAUSAL>(a, id);
-        // The item's first K tile goes out before its Q, which must wait until the
-        // previous item's products are done with the Q buffer. K then runs one tile
-        // ahead of V: K0, Q, K1, V0, K2, V1, ...
+        // The item's first K tile goes out before its Q. K then runs one tile ahead of V.
         if (!load_tile(it, 0, false)) { ok = false; break; }
-        if (q_cnt > 0 && !mbar_wait(bar(BAR_QE), (q_cnt - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(BAR_Q), 2 * TILE);
-        for (int t = 0; t < 2; ++t) {
+        // Q_t may be replaced once the previous item's last S_t has read it. Tile A
+        // finishes an item first, so Q_A goes out right away and Q_B after the
+        // item's first V tile: K0, Q_A, K1, V0, Q_B, K2, V1, ...
+        auto load_q = [&](int t) -> bool {
+          const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
+          if (q_cnt > 0 && !mbar_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
+          mbar_arrive_expect_tx(qf, TILE);
           for (int half = 0; half < 2; ++half) {
             const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
             if constexpr (CAUSAL)
-              tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, bar(BAR_Q));
+              tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, qf);
             else
-              tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, bar(BAR_Q));
+              tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, qf);
           }
-        }
-        ++q_cnt;
+          return true;
+        };
+        if (!load_q(0)) { ok = false; break; }
         for (int j = 0; ok && j < it.n_kv; ++j) {
           if (j + 1 < it.n_kv && !load_tile(it, j + 1, false)) ok = false;
           if (ok && !load_tile(it, j, true)) ok = false;
+          if (ok && j == 0 && !load_q(1)) ok = false;
         }
+        ++q_cnt;
       }
       if (!ok) fail(misc, a.err_flag);
       // Every issued copy must land before the CTA's shared memory is released
       // (immediate on the normal path, where the MMA warp already waited for them).
-      if (q_cnt > 0 && !mbar_wait(bar(BAR_Q), (q_cnt - 1) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      if (q_cnt > 0 && (!mbar_wait(bar(BAR_Q), (q_cnt - 1) & 1) || !mbar_wait(bar(BAR_Q1), (q_cnt - 1) & 1)))
+        set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
       for (uint32_t s = 0; s < NSK && s < k_cnt; ++s)
         if (!mbar_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
       for (uint32_t s = 0; s < NSV && s < v_cnt; ++s)
         if (!mbar_wait(bar(BAR_VF + s), ((v_cnt - 1 - s) / NSV) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One thread per query tile (warp 1: A, warp 2: B), so each tile's chain
+    // S -> softmax -> PV runs at its own pace, and tile A moves on to the next item
+    // while B finishes. They share only the K/V stages, whose release barriers take
+    // one arrival from each.
     if (lane == 0) {
+      const int t = warp - 1;
       const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
       const uint32_t idPV = idesc_bf16_f32(BM, HD, false, true);
       // Descriptors are built once; a K step inside a tile only moves the start
       // address, i.e. adds (byte offset >> 4) to the low field. The largest start
-      // (under 232 KB) plus the largest step stays inside the 14-bit field.
-      // Ring slots and the two Q tiles are TILE bytes apart, so a slot's descriptor is
-      // the first slot's plus slot * (TILE >> 4).
-      const uint64_t dq0 = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B);
+      // (under 232 KB) plus the largest step stays inside the 14-bit field. Ring slots
+      // and the two Q tiles are TILE bytes apart: slot i's descriptor is the first
+      // slot's plus i * (TILE >> 4).
+      constexpr uint64_t kSlot = TILE >> 4;
+      const uint64_t dq = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B) + (uint64_t)t * kSlot;
       const uint64_t dk0 = smem_desc(sb + SM_K, 16, 1024, kSwizzle128B);
       const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
-      constexpr uint64_t kSlot = TILE >> 4;
-      auto issue_s = [&](int t, uint32_t kg) {  // S_t = Q_t K^T, K at ring position kg
-        const uint64_t a0 = dq0 + (uint64_t)t * kSlot, b0 = dk0 + (uint64_t)(kg % NSK) * kSlot;
-        const uint32_t d = tmem + COL_S + t * BN;
+      const uint32_t d_s = tmem + COL_S + t * BN, d_o = tmem + COL_O + t * HD;
+      const uint32_t q_full = bar(t == 0 ? BAR_Q : BAR_Q1), q_empty = bar(BAR_QE + t);
+      auto issue_s = [&](uint32_t kg) {  // S_t = Q_t K^T, K at ring position kg
+        const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
-          mma_bf16_ss(d, a0 + off, b0 + off, idS, k > 0);
+          mma_bf16_ss(d_s, dq + off, b0 + off, idS, k > 0);
         }
         mma_commit(bar(BAR_SF + t));
       };
-      auto issue_pv = [&](int t, uint32_t vg, bool first) {  // O_t (+)= P_t V, V at ring position vg
+      auto issue_pv = [&](uint32_t vg, bool first) {  // O_t (+)= P_t V, V at ring position vg
         const uint64_t b0 = dv0 + (uint64_t)(vg % NSV) * kSlot;
-        const uint32_t d = tmem + COL_O + t * HD, pa = tmem + COL_S + t * BN;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_bf16_ts(d, pa + k * 8, b0 + (uint64_t)((k * 2048) >> 4), idPV, (!first || k > 0) ? 1u : 0u);
+          mma_bf16_ts(d_o, d_s + k * 8, b0 + (uint64_t)((k * 2048) >> 4), idPV, (!first || k > 0) ? 1u : 0u);
         mma_commit(bar(BAR_OD + t));
       };
-      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, pf_cnt[2] = {0, 0}, of_cnt[2] = {0, 0},
-               of_need[2] = {0, 0};
+      auto release = [&](uint32_t b, int n) {  // arrive n times once the products so far are done
+        for (int i = 0; i < n; ++i) mma_commit(b);
+      };
+      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, pf_cnt = 0, of_cnt = 0, of_need = 0;
       bool ok = true;
-      auto wait_k = [&](uint32_t kg) { return mbar_wait(bar(BAR_KF + kg % NSK), (kg / NSK) & 1); };
-      auto wait_v = [&](uint32_t vg) { return mbar_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1); };
       for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
         const Item it = make_item<CAUSAL>(a, id);
-        const bool has_b = it.B.n_tiles > 0;
-        const int lastA = it.A.n_tiles - 1;
+        const int n_t = (t == 0 ? it.A : it.B).n_tiles;  // key tiles this tile reads
+        const int n_o = (t == 0 ? it.B : it.A).n_tiles;  // key tiles the other tile reads
         const int n_kv = it.n_kv;
-        if (!mbar_wait(bar(BAR_Q), q_cnt & 1) || !wait_k(k_cnt)) { ok = false; break; }
+        // Only an issuer that reads a stage releases it. Where the other tile does not
+        // read stage j (j >= n_o), this issuer brings both arrivals, so a stage is never
+        // handed back to TMA while a product of either tile may still read it.
+        auto rel = [&](int j) { return j < n_o ? 1 : 2; };
+        if (n_t == 0) {  // only B can be missing: A covers the K/V arrivals
+          mma_commit(q_empty);  // its Q_B (never read) may be replaced
+          k_cnt += n_kv;
+          v_cnt += n_kv;
+          ++q_cnt;
+          continue;
+        }
+        if (!mbar_wait(q_full, q_cnt & 1) || !mbar_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
+          ok = false;
+          break;
+        }
         ++q_cnt;
         tc_fence_after();
-        issue_s(0, k_cnt);
-        if (has_b) issue_s(1, k_cnt);
-        mma_commit(bar(BAR_KE + k_cnt % NSK));  // K_0 is read by no later product
-        for (int j = 0; j < n_kv; ++j) {
+        issue_s(k_cnt);
+        if (n_t == 1) mma_commit(q_empty);  // the last product that reads this Q tile
+        release(bar(BAR_KE + k_cnt % NSK), rel(0));
+        for (int j = 0; j < n_t; ++j) {
           const uint32_t kg = k_cnt + j, vg = v_cnt + j;
-          bool v_ready = false;
-          if (j <= lastA) {
-            if (!mbar_wait(bar(BAR_PF + 0), pf_cnt[0] & 1)) { ok = false; break; }
-            ++pf_cnt[0];
-            // the previous item's epilogue must have read O_A before it is overwritten
-            if (j == 0 && of_need[0] > of_cnt[0]) {
-              if (!mbar_wait(bar(BAR_OF + 0), of_cnt[0] & 1)) { ok = false; break; }
-              ++of_cnt[0];
-            }
-            if (!wait_v(vg)) { ok = false; break; }
-            v_ready = true;
-            tc_fence_after();
-            issue_pv(0, vg, j == 0);
+          if (!mbar_wait(bar(BAR_PF + t), pf_cnt & 1)) { ok = false; break; }
+          ++pf_cnt;
+          // the previous item's epilogue must have read O before it is overwritten
+          if (j == 0 && of_need > of_cnt) {
+            if (!mbar_wait(bar(BAR_OF + t), of_cnt & 1)) { ok = false; break; }
+            ++of_cnt;
           }
-          if (j + 1 < n_kv) {
-            if (!wait_k(kg + 1)) { ok = false; break; }
+          if (!mbar_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(vg, j == 0);
+          release(bar(BAR_VE + vg % NSV), rel(j));
+          if (j + 1 < n_t) {
+            if (!mbar_wait(bar(BAR_KF + (kg + 1) % NSK), ((kg + 1) / NSK) & 1)) { ok = false; break; }
             tc_fence_after();
-            if (j + 1 <= lastA) issue_s(0, kg + 1);
-          }
-          if (has_b) {
-            if (!mbar_wait(bar(BAR_PF + 1), pf_cnt[1] & 1)) { ok = false; break; }
-            ++pf_cnt[1];
-            if (j == 0 && of_need[1] > of_cnt[1]) {
-              if (!mbar_wait(bar(BAR_OF + 1), of_cnt[1] & 1)) { ok = false; break; }
-              ++of_cnt[1];
-            }
-            if (!v_ready && !wait_v(vg)) { ok = false; break; }
-            tc_fence_after();
-            issue_pv(1, vg, j == 0);
-          }
-          mma_commit(bar(BAR_VE + vg % NSV));  // V_j is read by no later product
-          if (j + 1 < n_kv) {
-            if (has_b) issue_s(1, kg + 1);
-            mma_commit(bar(BAR_KE + (kg + 1) % NSK));  // nor is K_{j+1}
+            issue_s(kg + 1);
+            if (j + 1 == n_t - 1) mma_commit(q_empty);
+            release(bar(BAR_KE + (kg + 1) % NSK), rel(j + 1));
           }
         }
-        mma_commit(bar(BAR_QE));  // every product that reads Q of this item has been issued
         k_cnt += n_kv;
         v_cnt += n_kv;
-        ++of_need[0];
-        if (has_b) ++of_need[1];
+        ++of_need;
       }
       if (!ok) fail(misc, a.err_flag);
       // Every issued product must finish before TMEM is freed.
-      mma_commit(bar(BAR_DRAIN));
-      if (!mbar_wait(bar(BAR_DRAIN), 0)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      mma_commit(bar(BAR_DRAIN + t));
+      if (!mbar_wait(bar(BAR_DRAIN + t), 0)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp < 6) {
-    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + 0), bar(BAR_PF + 0), bar(BAR_OD + 0), bar(BAR_OF + 0),
-                         COL_S, COL_O, 0, n_items, warp, lane);
+  } else if (warp < 4) {  // warp 3 of warpgroup 0 has no role
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+    const int t = (warp - 4) / 4;
+    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + t), bar(BAR_PF + t), bar(BAR_ST + t), bar(BAR_IE + t),
+                         reinterpret_cast<float*>(smem + SM_INV) + t * BM, COL_S + t * BN,
+                         COL_O + t * HD, t, n_items, warp, lane);
   } else {
-    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + 1), bar(BAR_PF + 1), bar(BAR_OD + 1), bar(BAR_OF + 1),
-                         COL_S + BN, COL_O + HD, 1, n_items, warp, lane);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    uint32_t bars[8] = {bar(BAR_ST), bar(BAR_ST + 1), bar(BAR_OD),     bar(BAR_OD + 1),
+                        bar(BAR_OF), bar(BAR_OF + 1), bar(BAR_IE), bar(BAR_IE + 1)};
+    epilogue_loop<CAUSAL>(a, misc, bars, reinterpret_cast<const float*>(smem + SM_INV), n_items, warp,
+                          lane);
   }
 
   tc_fence_before();
