@@ -115,6 +115,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, ok);
 }
 
+// One lane of a converged warp, chosen by the hardware. The TMA and MMA warps run their
+// loops as whole warps (waits are warp-wide) and issue from an elected lane: a lone lane
+// in divergent code competes far worse with the ALU-heavy softmax warps for issue slots.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void fail(Misc* misc, int32_t* err) {
   misc->abort_ = 1;
   set_err(err, PKV_DEVERR_TIMEOUT);
@@ -447,10 +458,13 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      tma_prefetch_desc(&mq);
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
+    {
+      if (elect_one()) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+      }
+      __syncwarp();
       uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
       bool ok = true;
       // One 128-key tile of K or V (32 KiB) into its ring.
@@ -459,11 +473,16 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const uint32_t ns = is_v ? NSV : NSK;
         const uint32_t s = cnt % ns, u = cnt / ns;
         const uint32_t full = bar((is_v ? BAR_VF : BAR_KF) + s);
-        if (u > 0 && !mbar_wait(bar((is_v ? BAR_VE : BAR_KE) + s), (u - 1) & 1)) return false;
-        if (misc->abort_) return false;
-        mbar_arrive_expect_tx(full, TILE);
+        if (u > 0 && !warp_wait(bar((is_v ? BAR_VE : BAR_KE) + s), (u - 1) & 1)) return false;
+        if (__any_sync(0xffffffffu, misc->abort_ != 0)) return false;
         const uint32_t dst = sb + (is_v ? SM_V : SM_K) + s * TILE;
         const CUtensorMap* map = is_v ? &mv : &mk;
+        ++cnt;
+        if (!elect_one()) {
+          __syncwarp();
+          return true;
+        }
+        mbar_arrive_expect_tx(full, TILE);
         if constexpr (CAUSAL) {
           const int k0 = j * BN;
           tma_load_4d(dst, map, 0, it.hk, k0, it.b, full);
@@ -484,7 +503,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             tma_load_2d(dst + SUB + pp * 2048, map, 64, row, full);
           }
         }
-        ++cnt;
+        __syncwarp();
         return true;
       };
       for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
@@ -496,15 +515,18 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         // item's first V tile: K0, Q_A, K1, V0, Q_B, K2, V1, ...
         auto load_q = [&](int t) -> bool {
           const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
-          if (q_cnt > 0 && !mbar_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
-          mbar_arrive_expect_tx(qf, TILE);
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
-            if constexpr (CAUSAL)
-              tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, qf);
-            else
-              tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, qf);
+          if (q_cnt > 0 && !warp_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(qf, TILE);
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
+              if constexpr (CAUSAL)
+                tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, qf);
+              else
+                tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, qf);
+            }
           }
+          __syncwarp();
           return true;
         };
         if (!load_q(0)) { ok = false; break; }
@@ -515,15 +537,17 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         }
         ++q_cnt;
       }
-      if (!ok) fail(misc, a.err_flag);
+      if (!ok && lane == 0) fail(misc, a.err_flag);
       // Every issued copy must land before the CTA's shared memory is released
       // (immediate on the normal path, where the MMA warp already waited for them).
-      if (q_cnt > 0 && (!mbar_wait(bar(BAR_Q), (q_cnt - 1) & 1) || !mbar_wait(bar(BAR_Q1), (q_cnt - 1) & 1)))
-        set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      bool drained = true;
+      if (q_cnt > 0 && (!warp_wait(bar(BAR_Q), (q_cnt - 1) & 1) || !warp_wait(bar(BAR_Q1), (q_cnt - 1) & 1)))
+        drained = false;
       for (uint32_t s = 0; s < NSK && s < k_cnt; ++s)
-        if (!mbar_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+        if (!warp_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) drained = false;
       for (uint32_t s = 0; s < NSV && s < v_cnt; ++s)
-        if (!mbar_wait(bar(BAR_VF + s), ((v_cnt - 1 - s) / NSV) & 1)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+        if (!warp_wait(bar(BAR_VF + s), ((v_cnt - 1 - s) / NSV) & 1)) drained = false;
+      if (!drained && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA issuers
@@ -531,7 +555,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // S -> softmax -> PV runs at its own pace, and tile A moves on to the next item
     // while B finishes. They share only the K/V stages, whose release barriers take
     // one arrival from each.
-    if (lane == 0) {
+    {
       const int t = warp - 1;
       const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
       const uint32_t idPV = idesc_bf16_f32(BM, HD, false, true);
@@ -546,24 +570,34 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
       const uint32_t d_s = tmem + COL_S + t * BN, d_o = tmem + COL_O + t * HD;
       const uint32_t q_full = bar(t == 0 ? BAR_Q : BAR_Q1), q_empty = bar(BAR_QE + t);
-      auto issue_s = [&](uint32_t kg) {  // S_t = Q_t K^T, K at ring position kg
+      // S_t = Q_t K^T with K at ring position kg, then the K stage's release (rel
+      // arrivals) and, for the tile's last S, Q_t's release.
+      auto issue_s = [&](uint32_t kg, int rel_n, bool q_done) {
         const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
-          mma_bf16_ss(d_s, dq + off, b0 + off, idS, k > 0);
+          for (int k = 0; k < HD / 16; ++k) {
+            const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
+            mma_bf16_ss(d_s, dq + off, b0 + off, idS, k > 0);
+          }
+          mma_commit(bar(BAR_SF + t));
+          if (q_done) mma_commit(q_empty);  // the last product that reads this Q tile
+          for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_KE + kg % NSK));
         }
-        mma_commit(bar(BAR_SF + t));
+        __syncwarp();
       };
-      auto issue_pv = [&](uint32_t vg, bool first) {  // O_t (+)= P_t V, V at ring position vg
+      // O_t (+)= P_t V with V at ring position vg, then the V stage's release.
+      auto issue_pv = [&](uint32_t vg, bool first, int rel_n) {
         const uint64_t b0 = dv0 + (uint64_t)(vg % NSV) * kSlot;
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_bf16_ts(d_o, d_s + k * 8, b0 + (uint64_t)((k * 2048) >> 4), idPV, (!first || k > 0) ? 1u : 0u);
-        mma_commit(bar(BAR_OD + t));
-      };
-      auto release = [&](uint32_t b, int n) {  // arrive n times once the products so far are done
-        for (int i = 0; i < n; ++i) mma_commit(b);
+          for (int k = 0; k < BN / 16; ++k)
+            mma_bf16_ts(d_o, d_s + k * 8, b0 + (uint64_t)((k * 2048) >> 4), idPV,
+                        (!first || k > 0) ? 1u : 0u);
+          mma_commit(bar(BAR_OD + t));
+          for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_VE + vg % NSV));
+        }
+        __syncwarp();
       };
       uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, pf_cnt = 0, of_cnt = 0, of_need = 0;
       bool ok = true;
@@ -577,50 +611,47 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         // handed back to TMA while a product of either tile may still read it.
         auto rel = [&](int j) { return j < n_o ? 1 : 2; };
         if (n_t == 0) {  // only B can be missing: A covers the K/V arrivals
-          mma_commit(q_empty);  // its Q_B (never read) may be replaced
+          if (elect_one()) mma_commit(q_empty);  // its Q_B (never read) may be replaced
+          __syncwarp();
           k_cnt += n_kv;
           v_cnt += n_kv;
           ++q_cnt;
           continue;
         }
-        if (!mbar_wait(q_full, q_cnt & 1) || !mbar_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
+        if (!warp_wait(q_full, q_cnt & 1) || !warp_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
           ok = false;
           break;
         }
         ++q_cnt;
         tc_fence_after();
-        issue_s(k_cnt);
-        if (n_t == 1) mma_commit(q_empty);  // the last product that reads this Q tile
-        release(bar(BAR_KE + k_cnt % NSK), rel(0));
+        issue_s(k_cnt, rel(0), n_t == 1);
         for (int j = 0; j < n_t; ++j) {
           const uint32_t kg = k_cnt + j, vg = v_cnt + j;
-          if (!mbar_wait(bar(BAR_PF + t), pf_cnt & 1)) { ok = false; break; }
+          if (!warp_wait(bar(BAR_PF + t), pf_cnt & 1)) { ok = false; break; }
           ++pf_cnt;
           // the previous item's epilogue must have read O before it is overwritten
           if (j == 0 && of_need > of_cnt) {
-            if (!mbar_wait(bar(BAR_OF + t), of_cnt & 1)) { ok = false; break; }
+            if (!warp_wait(bar(BAR_OF + t), of_cnt & 1)) { ok = false; break; }
             ++of_cnt;
           }
-          if (!mbar_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
+          if (!warp_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(vg, j == 0);
-          release(bar(BAR_VE + vg % NSV), rel(j));
+          issue_pv(vg, j == 0, rel(j));
           if (j + 1 < n_t) {
-            if (!mbar_wait(bar(BAR_KF + (kg + 1) % NSK), ((kg + 1) / NSK) & 1)) { ok = false; break; }
+            if (!warp_wait(bar(BAR_KF + (kg + 1) % NSK), ((kg + 1) / NSK) & 1)) { ok = false; break; }
             tc_fence_after();
-            issue_s(kg + 1);
-            if (j + 1 == n_t - 1) mma_commit(q_empty);
-            release(bar(BAR_KE + (kg + 1) % NSK), rel(j + 1));
+            issue_s(kg + 1, rel(j + 1), j + 1 == n_t - 1);
           }
         }
         k_cnt += n_kv;
         v_cnt += n_kv;
         ++of_need;
       }
-      if (!ok) fail(misc, a.err_flag);
+      if (!ok && lane == 0) fail(misc, a.err_flag);
       // Every issued product must finish before TMEM is freed.
-      mma_commit(bar(BAR_DRAIN + t));
-      if (!mbar_wait(bar(BAR_DRAIN + t), 0)) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      if (elect_one()) mma_commit(bar(BAR_DRAIN + t));
+      __syncwarp();
+      if (!warp_wait(bar(BAR_DRAIN + t), 0) && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp < 4) {  // warp 3 of warpgroup 0 has no role
   } else if (warp < 12) {
