@@ -209,28 +209,30 @@ decode_paged_kernel(const DecodeArgs a) {
         flags->bad_page = 1;
       }
       const int cnt = min(32, n_pages - base);
+      // The whole warp runs the loop (the ring waits are warp-wide) and one elected
+      // lane issues each page's copies.
       for (int k = 0; k < cnt; ++k) {
         const int p = __shfl_sync(0xffffffffu, phys, k);
         const int i = base + k;
         const int s = i % C::NSTAGE;
         const int use = i / C::NSTAGE;
-        if (lane == 0) {
-          if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
-            ok = false;
-          } else if ((badm >> k) & 1u) {
+        if (use > 0 && !warp_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          if ((badm >> k) & 1u) {
             mbar_arrive(bar_full + 8 * s);  // completes the phase with no data
-            issued = i + 1;
           } else {
             const size_t off = ((size_t)p * a.n_kv_heads + g) * C::TILE;
             mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::TILE);
             bulk_g2s_hint(sbase + s * C::TILE, kbase + off, C::TILE, bar_full + 8 * s, pol);
             bulk_g2s_hint(sbase + (C::NSTAGE + s) * C::TILE, vbase + off, C::TILE,
                           bar_full + 8 * s, pol);
-            issued = i + 1;
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        __syncwarp();
+        issued = i + 1;
       }
     }
     if (lane == 0) {

@@ -108,24 +108,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// A wait taken by every lane of a warp; the result is the same on all lanes, so
-// the .sync.aligned tcgen05 instructions that follow never diverge.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// One lane of a converged warp, chosen by the hardware. The TMA and MMA warps run their
-// loops as whole warps (waits are warp-wide) and issue from an elected lane: a lone lane
-// in divergent code competes far worse with the ALU-heavy softmax warps for issue slots.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 __device__ __forceinline__ void fail(Misc* misc, int32_t* err) {
   misc->abort_ = 1;
   set_err(err, PKV_DEVERR_TIMEOUT);

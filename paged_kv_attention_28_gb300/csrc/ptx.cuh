@@ -69,6 +69,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// A wait taken by every lane of a warp; the result is the same on all lanes, so
+// .sync.aligned instructions that follow never diverge.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One lane of a converged warp, chosen by the hardware. Producer and MMA warps run
+// their loops as whole warps (waits are warp-wide) and issue from an elected lane: a
+// lone lane in divergent code competes far worse with ALU-heavy warps for issue slots.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // One-dimensional bulk copy global -> shared, completion counted in bytes on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
