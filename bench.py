@@ -363,7 +363,7 @@ def run_ours(args, rank, world, local):
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
     units = int(case.kv_lens.sum())
-    traffic = profiled_traffic(args.workload, source_hash("decode_kernel.cuh", "decode.cu"), units)
+    traffic = profiled_traffic(args.workload, source_hash("decode_kernel.cuh", "decode.cu", "ptx.cuh"), units)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
