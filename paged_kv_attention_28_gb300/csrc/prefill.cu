@@ -2,15 +2,16 @@
 //
 // Tiled FlashAttention ("快速注意力内核与算子融合", Q&A on FlashAttention): a CTA
 // owns two adjacent 128-row query tiles, A and B, of one (batch, head). It
-// walks the 128-key K/V tiles up to B's diagonal. For each tile it computes
-// S = Q K^T into tensor memory, updates the running row max and sum, writes
-// P = exp(S - m) back into tensor memory as bf16, and accumulates O += P V in
-// tensor memory. The T x T score matrix never leaves the chip. The causal mask
-// is applied by predication on the two diagonal tiles only.
+// walks the 128-key K/V tiles up to B's diagonal, each in two steps of 64 keys. For
+// each step it computes S = Q K^T into tensor memory, updates the running row max and
+// sum, writes P = exp(S - m) back into tensor memory as bf16, and accumulates O += P V
+// in tensor memory. The T x T score matrix never leaves the chip. The causal mask is
+// applied by predication on the two diagonal tiles only.
 //
-// A and B share every K/V tile that TMA brings in. Their softmax work
-// alternates with the tensor core: while one warpgroup turns S_A into P_A, the
-// tensor core runs B's products, and the other way round.
+// A and B share every K/V tile that TMA brings in. Each query tile has two S buffers,
+// so S for step s + 1 is computed while the softmax turns S_s into P_s: the chain
+// S -> softmax -> PV -> S that would otherwise serialise a tile is cut in two, and
+// the two tiles' products and softmaxes overlap.
 //
 // Warp roles (512 threads, four warpgroups):
 //   warpgroup 0: warp 0 TMA producer (Q_A and Q_B per item, K tiles into a 3-stage ring,
@@ -21,8 +22,9 @@
 //   warpgroup 3: epilogue: O / l out of TMEM to global memory, for both tiles
 // Registers are rebalanced with setmaxnreg: the softmax warpgroups get 168 per thread,
 // the other two 88 (88 + 168 + 168 + 88 = 512 per SM sub-partition, the launch's share).
-// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
-// P overwrites the first 64 columns of its own S buffer (packed bf16 pairs).
+// TMEM columns: S_A,0 [0,64), S_A,1 [64,128), S_B,0 [128,192), S_B,1 [192,256),
+// O_A [256,384), O_B [384,512). P overwrites the first 32 columns of its own S buffer
+// (packed bf16 pairs).
 // PV reads A = P from TMEM and B = V (MN-major) from shared memory.
 //
 // Lazy rescaling: a row keeps its reference max until a tile's max exceeds it
@@ -48,7 +50,8 @@ namespace pkv {
 namespace {
 
 constexpr int BM = 128;        // query rows per tile
-constexpr int BN = 128;        // keys per tile
+constexpr int BN = 128;        // keys per K/V tile
+constexpr int BS = 64;         // keys per S step (half a K/V tile)
 constexpr int HD = 128;        // head dim
 constexpr int SUB = 16384;     // one 128-row x 64-column bf16 sub-tile (128-byte swizzle)
 constexpr int TILE = 2 * SUB;  // 128 x 128 bf16
@@ -58,12 +61,13 @@ constexpr int SM_Q = 0;                      // Q_A, Q_B
 constexpr int SM_K = SM_Q + 2 * TILE;
 constexpr int SM_V = SM_K + NSK * TILE;
 constexpr int SM_BAR = SM_V + NSV * TILE;
-// barriers: q_full[2], k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2],
-// o_done[2], drain[2], q_empty[2] (products of an item done with a Q tile), o_free[2]
-// (epilogue read O). k_empty and v_empty take one arrival from each MMA issuer.
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 13,
-              BAR_OD = 15, BAR_DRAIN = 17, BAR_QE = 19, BAR_OF = 21, BAR_Q1 = 23, BAR_ST = 24, BAR_IE = 26,
-              NBAR = 28;
+// barriers: q_full[2], k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2 tiles][2
+// buffers], p_full[2][2], o_done[2] (one phase per PV step), drain[2], q_empty[2]
+// (products of an item done with a Q tile), o_free[2] (epilogue read O), o_item[2] (an
+// item's last PV finished). k_empty and v_empty take one arrival from each MMA issuer.
+constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 15,
+              BAR_OD = 19, BAR_DRAIN = 21, BAR_QE = 23, BAR_OF = 25, BAR_Q1 = 27, BAR_ST = 28, BAR_IE = 30,
+              BAR_OI = 32, NBAR = 34;
 // q_full and q_empty exist per query tile: tile t's Q uses BAR_Q / BAR_Q1 and BAR_QE + t.
 // st_full[2]: a tile's softmax has written its rows' 1/l for the epilogue warpgroup;
 // inv_empty[2]: the epilogue has read them, so the next item's softmax may overwrite them.
@@ -73,7 +77,7 @@ constexpr int SMEM_BYTES = SM_MISC + 64 + 1024;  // + slack to align the base to
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int THREADS = 512;  // four warpgroups; see the role list at the top
 constexpr int TMEM_COLS = 512;
-constexpr int COL_S = 0, COL_O = 256;
+constexpr int COL_S = 0, COL_O = 256;  // tile t: S buffers at t*128 + b*64, O at COL_O + t*128
 constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.0f;  // log2 units
@@ -198,11 +202,12 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
 }
 
 // The softmax warpgroup of one query tile of every item of this CTA: S -> P for each
-// key tile, then the epilogue. Phase counters run across items.
+// 64-key step, then the hand-off to the epilogue. Step g of the tile (counted across
+// items) uses S buffer g & 1 and barriers s_full[g & 1], p_full[g & 1].
 template <bool CAUSAL>
-__device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint32_t bar_sf,
-                                             uint32_t bar_pf, uint32_t bar_st, uint32_t bar_ie,
-                                             float* inv_rows,
+__device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint32_t bar_sf0,
+                                             uint32_t bar_pf0, uint32_t bar_od, uint32_t bar_st,
+                                             uint32_t bar_ie, float* inv_rows,
                                              uint32_t col_s, uint32_t col_o, int tile, int n_items,
                                              int warp, int lane) {
   const int quarter = warp & 3;
@@ -212,66 +217,65 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
   const uint32_t tO = misc->tmem_base + lane_addr + col_o;
   const float c = a.scale * kLog2eF;  // logits in log2 units: s * c
   const int H = a.n_qo_heads;
-  uint32_t sf_cnt = 0, st_cnt = 0;
+  uint32_t g = 0, st_cnt = 0;  // steps done (across items); items handed off
   bool ok = true;
   for (int id = blockIdx.x; id < n_items; id += gridDim.x) {
     const Item it = make_item<CAUSAL>(a, id);
     const TileJob& job = tile == 0 ? it.A : it.B;
-    const int n_tiles = job.n_tiles;
-    if (n_tiles == 0) continue;
+    const int n_steps = 2 * job.n_tiles;
+    if (n_steps == 0) continue;
     float ms = -INFINITY;  // reference max, log2 units
     float l = 0.0f;
-    for (int jj = 0; jj < n_tiles; ++jj) {
-      if (ok && !warp_wait(bar_sf, sf_cnt & 1)) ok = false;
-      ++sf_cnt;
+    for (int s = 0; s < n_steps; ++s, ++g) {
+      const uint32_t b = g & 1;
+      if (ok && !warp_wait(bar_sf0 + 8 * b, (g >> 1) & 1)) ok = false;
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(sr + 0));
-      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(sr + 64));
-      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(sr + 96));
+      const uint32_t tSb = tS + b * BS;
+      uint32_t sr[BS];
+      tmem_ld32(tSb + 0, *reinterpret_cast<uint32_t(*)[32]>(sr + 0));
+      tmem_ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_ld_wait();
       float* x = reinterpret_cast<float*>(sr);
-      if (jj == n_tiles - 1) {
-        // causal: key column i is visible to row r iff i <= r (diagonal tile);
-        // prefix: only the first last_valid keys of the last tile exist
-        const int limit = CAUSAL ? r + 1 : job.last_valid;
+      if (s >= n_steps - 2) {
+        // causal: key column k of the tile is visible to row r iff k <= r (diagonal
+        // tile); prefix: only the first last_valid keys of the last tile exist
+        const int limit = (CAUSAL ? r + 1 : job.last_valid) - (s & 1) * BS;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) x[i] = (i >= limit) ? -INFINITY : x[i];
+        for (int i = 0; i < BS; ++i) x[i] = (i >= limit) ? -INFINITY : x[i];
       }
       // row max over four independent chains
       float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]), m2 = fmaxf(x[4], x[5]),
             m3 = fmaxf(x[6], x[7]);
 #pragma unroll
-      for (int i = 8; i < 128; i += 8) {
+      for (int i = 8; i < BS; i += 8) {
         m0 = max3(m0, x[i], x[i + 1]);
         m1 = max3(m1, x[i + 2], x[i + 3]);
         m2 = max3(m2, x[i + 4], x[i + 5]);
         m3 = max3(m3, x[i + 6], x[i + 7]);
       }
+      // A fully masked step (the second half of a diagonal tile, rows < 64) has
+      // mt = -inf; it never comes first, so ms is finite by then.
       const float mt = max3(m0, m1, fmaxf(m2, m3)) * c;
-      const bool need = mt > ms + kRescaleSlack;  // always on the first tile (ms = -inf)
+      const bool need = mt > ms + kRescaleSlack;  // always on the first step (ms = -inf)
       const float m_new = need ? mt : ms;
       const float alpha = need ? ex2(ms - m_new) : 1.0f;
       const uint64_t cc = f2(c, c);
       const uint64_t mm = f2(-m_new, -m_new);
       uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-      // P in two halves of 32 packed columns; the S values are all in registers
-      // already, so P may overwrite the start of its own S buffer right away.
-#pragma unroll
-      for (int hlf = 0; hlf < 2; ++hlf) {
+      // P in 32 packed columns; the S values are all in registers already, so P may
+      // overwrite the start of its own S buffer right away.
+      {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int e = hlf * 64 + 2 * i;
           float y0, y1;
-          unf2(fma2(f2(x[e], x[e + 1]), cc, mm), y0, y1);
+          unf2(fma2(f2(x[2 * i], x[2 * i + 1]), cc, mm), y0, y1);
           const float p0 = ex2(y0), p1 = ex2(y1);
           acc[i & 3] = add2(acc[i & 3], f2(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tS + hlf * 32, pk);
+        tmem_st32(tSb, pk);
       }
       float s0, s1, s2, s3, s4, s5, s6, s7;
       unf2(acc[0], s0, s1);
@@ -279,9 +283,15 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
       unf2(acc[2], s4, s5);
       unf2(acc[3], s6, s7);
       l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
-      // S_j's completion implies PV_{j-1} has completed (the commit for S_j was
-      // issued after it), so O is stable here and P's columns are free.
-      if (jj > 0 && __any_sync(0xffffffffu, need)) {
+      // O changes only once PV_{g-1} has finished. S_g was issued after PV_{g-2} (within
+      // an item; across items after the previous item's last PV), and PV_g needs P_g,
+      // so PV_{g-1} is the only product pending on o_done: an exact phase wait.
+      if (s > 0 && __any_sync(0xffffffffu, need)) {
+        if (!warp_wait(bar_od, (g - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t o[32];
@@ -295,7 +305,7 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
       ms = m_new;
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_pf);
+      mbar_arrive(bar_pf0 + 8 * b);
     }
     // ---------------------------------------------------------------- hand-off
     // The row's LSE goes out here; 1/l goes to the epilogue warpgroup, which
@@ -330,19 +340,19 @@ __device__ __forceinline__ void epilogue_loop(const TileArgs& a, Misc* misc, uin
   const int r = quarter * 32 + lane;
   const uint32_t lane_addr = ((uint32_t)(quarter * 32) << 16);
   const int H = a.n_qo_heads;
-  uint32_t st_cnt[2] = {0, 0}, od_cnt[2] = {0, 0};
+  uint32_t st_cnt[2] = {0, 0}, oi_cnt[2] = {0, 0};
   bool ok = true;
   for (int id = blockIdx.x; id < n_items; id += gridDim.x) {
     const Item it = make_item<CAUSAL>(a, id);
     for (int t = 0; t < 2; ++t) {
       const TileJob& job = t == 0 ? it.A : it.B;
       if (job.n_tiles == 0) continue;
-      const uint32_t bar_st = bars[t], bar_od = bars[2 + t], bar_of = bars[4 + t], bar_ie = bars[6 + t];
-      od_cnt[t] += job.n_tiles;
-      // The softmax finished the item's last tile, so at most its last PV is pending.
+      const uint32_t bar_st = bars[t], bar_oi = bars[2 + t], bar_of = bars[4 + t], bar_ie = bars[6 + t];
       if (ok && !warp_wait(bar_st, st_cnt[t] & 1)) ok = false;
       ++st_cnt[t];
-      if (ok && !warp_wait(bar_od, (od_cnt[t] - 1) & 1)) ok = false;
+      // o_item has one phase per item: the next one needs this item's O freed first.
+      if (ok && !warp_wait(bar_oi, oi_cnt[t] & 1)) ok = false;
+      ++oi_cnt[t];
       tc_fence_after();
       if (!ok && lane == 0) fail(misc, a.err_flag);
       const float inv = ok ? inv_rows_base[t * BM + r] : NAN;
@@ -418,8 +428,8 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
-      const bool per_thread = (i == BAR_PF || i == BAR_PF + 1 || i == BAR_OF || i == BAR_OF + 1 ||
-                               i == BAR_ST || i == BAR_ST + 1 || i == BAR_IE || i == BAR_IE + 1);
+      const bool per_thread = (i >= BAR_PF && i < BAR_PF + 4) || i == BAR_OF || i == BAR_OF + 1 ||
+                              i == BAR_ST || i == BAR_ST + 1 || i == BAR_IE || i == BAR_IE + 1;
       const bool per_issuer = (i >= BAR_KE && i < BAR_KE + NSK) || (i >= BAR_VE && i < BAR_VE + NSV);
       mbar_init(bar(i), per_thread ? 128 : (per_issuer ? 2 : 1));
     }
@@ -539,7 +549,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     // one arrival from each.
     {
       const int t = warp - 1;
-      const uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+      const uint32_t idS = idesc_bf16_f32(BM, BS, false, false);
       const uint32_t idPV = idesc_bf16_f32(BM, HD, false, true);
       // Descriptors are built once; a K step inside a tile only moves the start
       // address, i.e. adds (byte offset >> 4) to the low field. The largest start
@@ -552,36 +562,40 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
       const uint32_t d_s = tmem + COL_S + t * BN, d_o = tmem + COL_O + t * HD;
       const uint32_t q_full = bar(t == 0 ? BAR_Q : BAR_Q1), q_empty = bar(BAR_QE + t);
-      // S_t = Q_t K^T with K at ring position kg, then the K stage's release (rel
-      // arrivals) and, for the tile's last S, Q_t's release.
-      auto issue_s = [&](uint32_t kg, int rel_n, bool q_done) {
-        const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot;
+      // S for global step gs (keys [64*half, 64*half + 64) of the K tile at ring position
+      // kg) into S buffer gs & 1; then the K stage's release (rel arrivals) after the
+      // tile's second half, and Q_t's release after the item's last step.
+      auto issue_s = [&](uint32_t gs, uint32_t kg, int half, int rel_n, bool q_done) {
+        const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot + (uint64_t)((half * BS * 128) >> 4);
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < HD / 16; ++k) {
             const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
-            mma_bf16_ss(d_s, dq + off, b0 + off, idS, k > 0);
+            mma_bf16_ss(d_s + (gs & 1) * BS, dq + off, b0 + off, idS, k > 0);
           }
-          mma_commit(bar(BAR_SF + t));
+          mma_commit(bar(BAR_SF + 2 * t + (gs & 1)));
           if (q_done) mma_commit(q_empty);  // the last product that reads this Q tile
           for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_KE + kg % NSK));
         }
         __syncwarp();
       };
-      // O_t (+)= P_t V with V at ring position vg, then the V stage's release.
-      auto issue_pv = [&](uint32_t vg, bool first, int rel_n) {
+      // O_t (+)= P_gp V over keys [64*half, +64) of the V tile at ring position vg; then
+      // o_done, the V stage's release after the tile's second half, o_item after the
+      // item's last step.
+      auto issue_pv = [&](uint32_t gp, uint32_t vg, int half, bool first, int rel_n, bool last) {
         const uint64_t b0 = dv0 + (uint64_t)(vg % NSV) * kSlot;
         if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            mma_bf16_ts(d_o, d_s + k * 8, b0 + (uint64_t)((k * 2048) >> 4), idPV,
-                        (!first || k > 0) ? 1u : 0u);
+          for (int k = 0; k < BS / 16; ++k)
+            mma_bf16_ts(d_o, d_s + (gp & 1) * BS + k * 8, b0 + (uint64_t)(((half * 4 + k) * 2048) >> 4),
+                        idPV, (!first || k > 0) ? 1u : 0u);
           mma_commit(bar(BAR_OD + t));
           for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_VE + vg % NSV));
+          if (last) mma_commit(bar(BAR_OI + t));
         }
         __syncwarp();
       };
-      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, pf_cnt = 0, of_cnt = 0, of_need = 0;
+      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, g = 0, of_cnt = 0, of_need = 0;
       bool ok = true;
       for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
         const Item it = make_item<CAUSAL>(a, id);
@@ -600,29 +614,36 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           ++q_cnt;
           continue;
         }
+        const int n_s = 2 * n_t;  // 64-key steps
         if (!warp_wait(q_full, q_cnt & 1) || !warp_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
           ok = false;
           break;
         }
         ++q_cnt;
         tc_fence_after();
-        issue_s(k_cnt, rel(0), n_t == 1);
-        for (int j = 0; j < n_t; ++j) {
-          const uint32_t kg = k_cnt + j, vg = v_cnt + j;
-          if (!warp_wait(bar(BAR_PF + t), pf_cnt & 1)) { ok = false; break; }
-          ++pf_cnt;
+        // S for the first two steps (both halves of K tile 0); the buffers were last read
+        // by the previous item's last two PV products, issued earlier by this thread.
+        issue_s(g, k_cnt, 0, 0, false);
+        issue_s(g + 1, k_cnt, 1, rel(0), n_s == 2);
+        for (int st = 0; st < n_s; ++st, ++g) {
+          const int j = st >> 1, half = st & 1;
+          if (!warp_wait(bar(BAR_PF + 2 * t + (g & 1)), (g >> 1) & 1)) { ok = false; break; }
           // the previous item's epilogue must have read O before it is overwritten
-          if (j == 0 && of_need > of_cnt) {
+          if (st == 0 && of_need > of_cnt) {
             if (!warp_wait(bar(BAR_OF + t), of_cnt & 1)) { ok = false; break; }
             ++of_cnt;
           }
-          if (!warp_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
+          const uint32_t vg = v_cnt + j;
+          if (half == 0 && !warp_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(vg, j == 0, rel(j));
-          if (j + 1 < n_t) {
-            if (!warp_wait(bar(BAR_KF + (kg + 1) % NSK), ((kg + 1) / NSK) & 1)) { ok = false; break; }
+          issue_pv(g, vg, half, st == 0, half == 1 ? rel(j) : 0, st == n_s - 1);
+          // S two steps ahead reuses P_g's buffer: the in-order tensor pipe reads P_g first.
+          const int sn = st + 2;
+          if (sn < n_s) {
+            const uint32_t kg = k_cnt + (sn >> 1);
+            if ((sn & 1) == 0 && !warp_wait(bar(BAR_KF + kg % NSK), (kg / NSK) & 1)) { ok = false; break; }
             tc_fence_after();
-            issue_s(kg + 1, rel(j + 1), j + 1 == n_t - 1);
+            issue_s(g + 2, kg, sn & 1, (sn & 1) ? rel(sn >> 1) : 0, sn == n_s - 1);
           }
         }
         k_cnt += n_kv;
@@ -639,12 +660,13 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
     const int t = (warp - 4) / 4;
-    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + t), bar(BAR_PF + t), bar(BAR_ST + t), bar(BAR_IE + t),
+    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + 2 * t), bar(BAR_PF + 2 * t), bar(BAR_OD + t),
+                         bar(BAR_ST + t), bar(BAR_IE + t),
                          reinterpret_cast<float*>(smem + SM_INV) + t * BM, COL_S + t * BN,
                          COL_O + t * HD, t, n_items, warp, lane);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
-    uint32_t bars[8] = {bar(BAR_ST), bar(BAR_ST + 1), bar(BAR_OD),     bar(BAR_OD + 1),
+    uint32_t bars[8] = {bar(BAR_ST), bar(BAR_ST + 1), bar(BAR_OI),     bar(BAR_OI + 1),
                         bar(BAR_OF), bar(BAR_OF + 1), bar(BAR_IE), bar(BAR_IE + 1)};
     epilogue_loop<CAUSAL>(a, misc, bars, reinterpret_cast<const float*>(smem + SM_INV), n_items, warp,
                           lane);
