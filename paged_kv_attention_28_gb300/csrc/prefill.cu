@@ -14,9 +14,10 @@
 // the two tiles' products and softmaxes overlap.
 //
 // Warp roles (512 threads, four warpgroups):
-//   warpgroup 0: warp 0 TMA producer (Q_A and Q_B per item, K tiles into a 3-stage ring,
-//                V tiles into a 2-stage ring; owns TMEM), warps 1 and 2 MMA issuers of
-//                tiles A and B (one thread each), warp 3 idle
+//   warpgroup 0: warp 0 TMA producer of Q_A, Q_B (per item) and K tiles (3-stage ring;
+//                owns TMEM), warp 3 TMA producer of V tiles (2-stage ring), warps 1 and
+//                2 MMA issuers of tiles A and B. All four run their loops as whole warps
+//                and issue from an elected lane.
 //   warpgroup 1: softmax of tile A, one thread per row (warp w reads TMEM lanes 32*(w%4)..)
 //   warpgroup 2: softmax of tile B
 //   warpgroup 3: epilogue: O / l out of TMEM to global memory, for both tiles
@@ -448,8 +449,10 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   // Registers are rebalanced between warpgroups at the head of each role (setmaxnreg is
   // warpgroup-wide: every warp of a warpgroup executes the same one).
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 0 streams Q and K tiles, warp 3 the V tiles: each waits only on its own
+    // ring, so a tile's next item can start while the other tile still drains V.
     {
       if (elect_one()) {
         tma_prefetch_desc(&mq);
@@ -457,6 +460,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         tma_prefetch_desc(&mv);
       }
       __syncwarp();
+      const bool v_role = warp == 3;
       uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
       bool ok = true;
       // One 128-key tile of K or V (32 KiB) into its ring.
@@ -500,11 +504,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       };
       for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
         const Item it = make_item<CAUSAL>(a, id);
-        // The item's first K tile goes out before its Q. K then runs one tile ahead of V.
-        if (!load_tile(it, 0, false)) { ok = false; break; }
-        // Q_t may be replaced once the previous item's last S_t has read it. Tile A
-        // finishes an item first, so Q_A goes out right away and Q_B after the
-        // item's first V tile: K0, Q_A, K1, V0, Q_B, K2, V1, ...
+        // Q_t may be replaced once the previous item's last S_t has read it.
         auto load_q = [&](int t) -> bool {
           const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
           if (q_cnt > 0 && !warp_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
@@ -521,13 +521,14 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           __syncwarp();
           return true;
         };
-        if (!load_q(0)) { ok = false; break; }
-        for (int j = 0; ok && j < it.n_kv; ++j) {
-          if (j + 1 < it.n_kv && !load_tile(it, j + 1, false)) ok = false;
-          if (ok && !load_tile(it, j, true)) ok = false;
-          if (ok && j == 0 && !load_q(1)) ok = false;
+        if (v_role) {
+          for (int j = 0; ok && j < it.n_kv; ++j) ok = load_tile(it, j, true);
+        } else {
+          // Q_A, K0, Q_B, K1, K2, ...: both tiles can start as soon as K0 is in.
+          ok = load_q(0) && load_tile(it, 0, false) && load_q(1);
+          for (int j = 1; ok && j < it.n_kv; ++j) ok = load_tile(it, j, false);
+          ++q_cnt;
         }
-        ++q_cnt;
       }
       if (!ok && lane == 0) fail(misc, a.err_flag);
       // Every issued copy must land before the CTA's shared memory is released
@@ -656,7 +657,6 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       __syncwarp();
       if (!warp_wait(bar(BAR_DRAIN + t), 0) && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp < 4) {  // warp 3 of warpgroup 0 has no role
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
     const int t = (warp - 4) / 4;
