@@ -39,10 +39,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 // far below FLT_MAX, and a chunk 60 below the reference contributes < e^-60.
 constexpr float kUnifiedBeta = 60.0f;
 
-template <typename T, int D, int P, int G>
+// Lanes per token row: 16 halves the registers a lane holds for G >= 4 (q and the
+// accumulators of G heads), so that G = 4 fits three CTAs per SM; the unified-max
+// variant of G = 4 measured faster with 8 lanes and two CTAs per SM.
+template <typename T, int D, int P, int G, bool UNIFIED = false>
 struct DecodeCfg {
   static constexpr int ES = sizeof(T);
-  static constexpr int LPT = (G >= 8) ? 16 : 8;   // lanes that share one token row
+  static constexpr int LPT = (G >= 8 || (G == 4 && !UNIFIED)) ? 16 : 8;
   static constexpr int TPI = 32 / LPT;             // token rows a warp covers per step
   static constexpr int DPL = D / LPT;              // head dims held per lane
   static constexpr int VEC = (16 / ES < DPL) ? 16 / ES : DPL;  // elements per smem load
@@ -55,7 +58,7 @@ struct DecodeCfg {
   static constexpr int NW = 4;                     // consumer warps
   static constexpr int NSTAGE = 8;                 // ring depth (multiple of NW)
   static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int MIN_BLOCKS = (G >= 4) ? 2 : 3;
+  static constexpr int MIN_BLOCKS = (G >= 8 || (G == 4 && UNIFIED)) ? 2 : 3;
   static constexpr int BAR_OFF = 2 * NSTAGE * TILE;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NSTAGE * 8;
   static constexpr int SMEM = FLAG_OFF + 16;
@@ -145,9 +148,9 @@ __device__ void write_group_const(const DecodeArgs& a, int b, int g, float o, fl
 }
 
 template <typename T, int D, int P, int G, bool UNIFIED>
-__global__ void __launch_bounds__(DecodeCfg<T, D, P, G>::THREADS, DecodeCfg<T, D, P, G>::MIN_BLOCKS)
+__global__ void __launch_bounds__(DecodeCfg<T, D, P, G, UNIFIED>::THREADS, DecodeCfg<T, D, P, G, UNIFIED>::MIN_BLOCKS)
 decode_paged_kernel(const DecodeArgs a) {
-  using C = DecodeCfg<T, D, P, G>;
+  using C = DecodeCfg<T, D, P, G, UNIFIED>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int split = blockIdx.x;
   const int g = blockIdx.y;
@@ -518,7 +521,7 @@ decode_paged_kernel(const DecodeArgs a) {
 
 template <typename T, int D, int P, int G, bool UNIFIED>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  using C = DecodeCfg<T, D, P, G>;
+  using C = DecodeCfg<T, D, P, G, UNIFIED>;
   auto kern = decode_paged_kernel<T, D, P, G, UNIFIED>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
