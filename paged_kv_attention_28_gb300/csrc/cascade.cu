@@ -7,6 +7,7 @@
 // sharing in the paged cache ("快速注意力内核与算子融合", Q&A on paged attention).
 // The combination is the log-sum-exp merge of partial states that FlashDecoding
 // performs at the end ("【FlashAttention-V4，非官方】FlashDecoding++", section 1).
+#include <mutex>
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -66,8 +67,8 @@ int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_q
   if (sms <= 0) sms = 148;
   // About half the SMs for the prefix, and at least four key tiles per chunk so that
   // each CTA's query load and partial-state write are amortised.
-  long want = (sms / 2) / ((long)n_kv_heads * row_pairs);
-  const long max_chunks = (n_tiles + 3) / 4;
+  long want = sms / ((long)n_kv_heads * row_pairs);
+  const long max_chunks = (n_tiles + 1) / 2;
   if (want > max_chunks) want = max_chunks;
   if (want < 1) want = 1;
   const int tpc = (int)((n_tiles + want - 1) / want);
@@ -88,11 +89,50 @@ SplitPlan cascade_suffix_plan(int n_requests, int max_suffix_blocks, int n_qo_he
   return p;
 }
 
+namespace {
+
+// A side stream and two events per device, created once and kept for the life of the
+// process: the prefix kernel runs on the side stream beside the suffix decode, joined
+// back into the caller's stream by events (which also works inside a stream capture).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+int side_stream_for_current_device(SideStream** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    if (check_launch(cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != PKV_OK ||
+        check_launch(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != PKV_OK ||
+        check_launch(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != PKV_OK)
+      return PKV_ERR_LAUNCH;
+  }
+  *out = &ss;
+  return PKV_OK;
+}
+
+}  // namespace
+
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream) {
-  // 1) the shared prefix, once per KV head for all requests (tensor cores)
+  // 1) the shared prefix, once per KV head for all requests (tensor cores), on the side
+  //    stream: it uses few CTAs, and the suffix decode below fills the other SMs.
+  SideStream* side = nullptr;
   if (a.prefix_len > 0) {
-    const int rc = launch_cascade_prefix(a, stream);
+    int rc = side_stream_for_current_device(&side);
     if (rc != PKV_OK) return rc;
+    // One cascade at a time may use the side stream's events.
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    if (check_launch(cudaEventRecord(side->fork, stream)) != PKV_OK ||
+        check_launch(cudaStreamWaitEvent(side->s, side->fork, 0)) != PKV_OK)
+      return PKV_ERR_LAUNCH;
+    rc = launch_cascade_prefix(a, side->s);
+    if (rc != PKV_OK) return rc;
+    if (check_launch(cudaEventRecord(side->join, side->s)) != PKV_OK) return PKV_ERR_LAUNCH;
   }
   // 2) every request's own suffix pages: fp32 partial states, one per live split
   DecodeArgs d{};
@@ -118,6 +158,7 @@ int launch_cascade(const CascadeArgs& a, cudaStream_t stream) {
   d.partial_only = true;
   int rc = launch_decode_partials(d, stream);
   if (rc != PKV_OK) return rc;
+  if (side && check_launch(cudaStreamWaitEvent(stream, side->join, 0)) != PKV_OK) return PKV_ERR_LAUNCH;
   // 3) merge
   const int rows = a.n_requests * a.n_qo_heads;
   if (a.head_dim != 128) return PKV_ERR_UNSUPPORTED;
