@@ -11,7 +11,9 @@
  * --------------------------------
  * - Pointers named q, k*, v*, out*, lse*, block_table*, kv_lens*, *_lens,
  *   workspace and err_flag are DEVICE pointers. The caller owns them. The
- *   library never allocates, frees, copies to the host or synchronises.
+ *   library never allocates or frees device memory, copies to the host or
+ *   synchronises (attn_decode_cascade keeps one side stream and two events per
+ *   device, created on first use).
  * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *   stream. All work is enqueued on it asynchronously. Outputs are valid once
  *   the caller has synchronised with that stream.
@@ -252,6 +254,11 @@ size_t attn_cascade_workspace_size(int n_requests, int prefix_len, int max_suffi
  *   workspace          : >= attn_cascade_workspace_size bytes, 256-byte aligned
  * The result equals attn_decode_paged over the concatenated sequences, up to
  * rounding.
+ *
+ * The prefix product runs on a side stream of the library's (one per device,
+ * created with two events on first use and kept for the life of the process),
+ * forked from and joined back into `stream` with events, so that it overlaps the
+ * suffix decode; the call still completes in `stream` order and may be captured.
  */
 int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
                         const int32_t* prefix_block_table, int prefix_len,
