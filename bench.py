@@ -195,6 +195,12 @@ def barrier(world):
         dist.barrier()
 
 
+def weak_scaling_rate(units_per_step, steps, world, seconds):
+    """Whole-job throughput of `world` replicas that each process `units_per_step` per step
+    for `steps` steps: every rank's units over the slowest rank's time (max over ranks)."""
+    return units_per_step * steps * world / seconds
+
+
 def max_over_ranks(x, world):
     if world == 1:
         return x
@@ -329,7 +335,7 @@ def run_ours(args, rank, world, local):
     times_ms = [a.elapsed_time(b) for a, b in ev]
     total_s = sum(times_ms) / 1e3
     total_s = max_over_ranks(total_s, world)
-    value = algo_bytes * args.steps * world / total_s / 1e9
+    value = weak_scaling_rate(algo_bytes, args.steps, world, total_s) / 1e9
     ms_per_step = 1000 * total_s / args.steps
     kernel_gbs = algo_bytes / (statistics.mean(times_ms) / 1e3) / 1e9
 
@@ -358,7 +364,7 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    e2e_value = algo_bytes * e2e_steps * world / e2e_s / 1e9
+    e2e_value = weak_scaling_rate(algo_bytes, e2e_steps, world, e2e_s) / 1e9
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_lens))
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
 
