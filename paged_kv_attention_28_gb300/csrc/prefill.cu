@@ -446,216 +446,221 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
-  // Registers are rebalanced between warpgroups at the head of each role (setmaxnreg is
-  // warpgroup-wide: every warp of a warpgroup executes the same one).
-  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
-  if (warp == 0 || warp == 3) {
-    // ------------------------------------------------------------------ TMA producers
-    // Warp 0 streams Q and K tiles, warp 3 the V tiles: each waits only on its own
-    // ring, so a tile's next item can start while the other tile still drains V.
-    {
-      if (elect_one()) {
-        tma_prefetch_desc(&mq);
-        tma_prefetch_desc(&mk);
-        tma_prefetch_desc(&mv);
-      }
-      __syncwarp();
-      const bool v_role = warp == 3;
-      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
-      bool ok = true;
-      // One 128-key tile of K or V (32 KiB) into its ring.
-      auto load_tile = [&](const Item& it, int j, bool is_v) -> bool {
-        uint32_t& cnt = is_v ? v_cnt : k_cnt;
-        const uint32_t ns = is_v ? NSV : NSK;
-        const uint32_t s = cnt % ns, u = cnt / ns;
-        const uint32_t full = bar((is_v ? BAR_VF : BAR_KF) + s);
-        if (u > 0 && !warp_wait(bar((is_v ? BAR_VE : BAR_KE) + s), (u - 1) & 1)) return false;
-        if (__any_sync(0xffffffffu, misc->abort_ != 0)) return false;
-        const uint32_t dst = sb + (is_v ? SM_V : SM_K) + s * TILE;
-        const CUtensorMap* map = is_v ? &mv : &mk;
-        ++cnt;
-        if (!elect_one()) {
-          __syncwarp();
-          return true;
-        }
-        mbar_arrive_expect_tx(full, TILE);
-        if constexpr (CAUSAL) {
-          const int k0 = j * BN;
-          tma_load_4d(dst, map, 0, it.hk, k0, it.b, full);
-          tma_load_4d(dst + SUB, map, 64, it.hk, k0, it.b, full);
-        } else {
-          // Eight pages of 16 keys make one 128-key tile; each page is a 16-row box.
-          // Slots past the prefix reload its first page (finite data; masked out).
-          for (int pp = 0; pp < 8; ++pp) {
-            const int page_idx = (it.kv_first + j) * 8 + pp;
-            int phys = __ldg(a.prefix_table + (page_idx < a.n_prefix_pages ? page_idx : 0));
-            if (phys < 0 || phys >= a.num_pages) {
-              misc->bad_page = 1;
-              set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
-              phys = 0;
-            }
-            const int row = (phys * a.n_kv_heads + it.hk) * 16;
-            tma_load_2d(dst + pp * 2048, map, 0, row, full);
-            tma_load_2d(dst + SUB + pp * 2048, map, 64, row, full);
-          }
+  // Registers are rebalanced between warpgroups with setmaxnreg, which every warp of a
+  // warpgroup executes at the same instruction. Each warpgroup's code sits in one
+  // branch that starts with its setmaxnreg, so the compiler allocates that code within
+  // the new limit: code the instruction does not dominate may use registers that the
+  // instruction has already released.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
+    if (warp == 0 || warp == 3) {
+      // ------------------------------------------------------------------ TMA producers
+      // Warp 0 streams Q and K tiles, warp 3 the V tiles: each waits only on its own
+      // ring, so a tile's next item can start while the other tile still drains V.
+      {
+        if (elect_one()) {
+          tma_prefetch_desc(&mq);
+          tma_prefetch_desc(&mk);
+          tma_prefetch_desc(&mv);
         }
         __syncwarp();
-        return true;
-      };
-      for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
-        const Item it = make_item<CAUSAL>(a, id);
-        // Q_t may be replaced once the previous item's last S_t has read it.
-        auto load_q = [&](int t) -> bool {
-          const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
-          if (q_cnt > 0 && !warp_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
-          if (elect_one()) {
-            mbar_arrive_expect_tx(qf, TILE);
-            for (int half = 0; half < 2; ++half) {
-              const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
-              if constexpr (CAUSAL)
-                tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, qf);
-              else
-                tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, qf);
+        const bool v_role = warp == 3;
+        uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
+        bool ok = true;
+        // One 128-key tile of K or V (32 KiB) into its ring.
+        auto load_tile = [&](const Item& it, int j, bool is_v) -> bool {
+          uint32_t& cnt = is_v ? v_cnt : k_cnt;
+          const uint32_t ns = is_v ? NSV : NSK;
+          const uint32_t s = cnt % ns, u = cnt / ns;
+          const uint32_t full = bar((is_v ? BAR_VF : BAR_KF) + s);
+          if (u > 0 && !warp_wait(bar((is_v ? BAR_VE : BAR_KE) + s), (u - 1) & 1)) return false;
+          if (__any_sync(0xffffffffu, misc->abort_ != 0)) return false;
+          const uint32_t dst = sb + (is_v ? SM_V : SM_K) + s * TILE;
+          const CUtensorMap* map = is_v ? &mv : &mk;
+          ++cnt;
+          if (!elect_one()) {
+            __syncwarp();
+            return true;
+          }
+          mbar_arrive_expect_tx(full, TILE);
+          if constexpr (CAUSAL) {
+            const int k0 = j * BN;
+            tma_load_4d(dst, map, 0, it.hk, k0, it.b, full);
+            tma_load_4d(dst + SUB, map, 64, it.hk, k0, it.b, full);
+          } else {
+            // Eight pages of 16 keys make one 128-key tile; each page is a 16-row box.
+            // Slots past the prefix reload its first page (finite data; masked out).
+            for (int pp = 0; pp < 8; ++pp) {
+              const int page_idx = (it.kv_first + j) * 8 + pp;
+              int phys = __ldg(a.prefix_table + (page_idx < a.n_prefix_pages ? page_idx : 0));
+              if (phys < 0 || phys >= a.num_pages) {
+                misc->bad_page = 1;
+                set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
+                phys = 0;
+              }
+              const int row = (phys * a.n_kv_heads + it.hk) * 16;
+              tma_load_2d(dst + pp * 2048, map, 0, row, full);
+              tma_load_2d(dst + SUB + pp * 2048, map, 64, row, full);
             }
           }
           __syncwarp();
           return true;
         };
-        if (v_role) {
-          for (int j = 0; ok && j < it.n_kv; ++j) ok = load_tile(it, j, true);
-        } else {
-          // Q_A, K0, Q_B, K1, K2, ...: both tiles can start as soon as K0 is in.
-          ok = load_q(0) && load_tile(it, 0, false) && load_q(1);
-          for (int j = 1; ok && j < it.n_kv; ++j) ok = load_tile(it, j, false);
-          ++q_cnt;
-        }
-      }
-      if (!ok && lane == 0) fail(misc, a.err_flag);
-      // Every issued copy must land before the CTA's shared memory is released
-      // (immediate on the normal path, where the MMA warp already waited for them).
-      bool drained = true;
-      if (q_cnt > 0 && (!warp_wait(bar(BAR_Q), (q_cnt - 1) & 1) || !warp_wait(bar(BAR_Q1), (q_cnt - 1) & 1)))
-        drained = false;
-      for (uint32_t s = 0; s < NSK && s < k_cnt; ++s)
-        if (!warp_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) drained = false;
-      for (uint32_t s = 0; s < NSV && s < v_cnt; ++s)
-        if (!warp_wait(bar(BAR_VF + s), ((v_cnt - 1 - s) / NSV) & 1)) drained = false;
-      if (!drained && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
-    }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------------ MMA issuers
-    // One thread per query tile (warp 1: A, warp 2: B), so each tile's chain
-    // S -> softmax -> PV runs at its own pace, and tile A moves on to the next item
-    // while B finishes. They share only the K/V stages, whose release barriers take
-    // one arrival from each.
-    {
-      const int t = warp - 1;
-      const uint32_t idS = idesc_bf16_f32(BM, BS, false, false);
-      const uint32_t idPV = idesc_bf16_f32(BM, HD, false, true);
-      // Descriptors are built once; a K step inside a tile only moves the start
-      // address, i.e. adds (byte offset >> 4) to the low field. The largest start
-      // (under 232 KB) plus the largest step stays inside the 14-bit field. Ring slots
-      // and the two Q tiles are TILE bytes apart: slot i's descriptor is the first
-      // slot's plus i * (TILE >> 4).
-      constexpr uint64_t kSlot = TILE >> 4;
-      const uint64_t dq = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B) + (uint64_t)t * kSlot;
-      const uint64_t dk0 = smem_desc(sb + SM_K, 16, 1024, kSwizzle128B);
-      const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
-      const uint32_t d_s = tmem + COL_S + t * BN, d_o = tmem + COL_O + t * HD;
-      const uint32_t q_full = bar(t == 0 ? BAR_Q : BAR_Q1), q_empty = bar(BAR_QE + t);
-      // S for global step gs (keys [64*half, 64*half + 64) of the K tile at ring position
-      // kg) into S buffer gs & 1; then the K stage's release (rel arrivals) after the
-      // tile's second half, and Q_t's release after the item's last step.
-      auto issue_s = [&](uint32_t gs, uint32_t kg, int half, int rel_n, bool q_done) {
-        const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot + (uint64_t)((half * BS * 128) >> 4);
-        if (elect_one()) {
-#pragma unroll
-          for (int k = 0; k < HD / 16; ++k) {
-            const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
-            mma_bf16_ss(d_s + (gs & 1) * BS, dq + off, b0 + off, idS, k > 0);
+        for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
+          const Item it = make_item<CAUSAL>(a, id);
+          // Q_t may be replaced once the previous item's last S_t has read it.
+          auto load_q = [&](int t) -> bool {
+            const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
+            if (q_cnt > 0 && !warp_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
+            if (elect_one()) {
+              mbar_arrive_expect_tx(qf, TILE);
+              for (int half = 0; half < 2; ++half) {
+                const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
+                if constexpr (CAUSAL)
+                  tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, qf);
+                else
+                  tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, qf);
+              }
+            }
+            __syncwarp();
+            return true;
+          };
+          if (v_role) {
+            for (int j = 0; ok && j < it.n_kv; ++j) ok = load_tile(it, j, true);
+          } else {
+            // Q_A, K0, Q_B, K1, K2, ...: both tiles can start as soon as K0 is in.
+            ok = load_q(0) && load_tile(it, 0, false) && load_q(1);
+            for (int j = 1; ok && j < it.n_kv; ++j) ok = load_tile(it, j, false);
+            ++q_cnt;
           }
-          mma_commit(bar(BAR_SF + 2 * t + (gs & 1)));
-          if (q_done) mma_commit(q_empty);  // the last product that reads this Q tile
-          for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_KE + kg % NSK));
         }
-        __syncwarp();
-      };
-      // O_t (+)= P_gp V over keys [64*half, +64) of the V tile at ring position vg; then
-      // o_done, the V stage's release after the tile's second half, o_item after the
-      // item's last step.
-      auto issue_pv = [&](uint32_t gp, uint32_t vg, int half, bool first, int rel_n, bool last) {
-        const uint64_t b0 = dv0 + (uint64_t)(vg % NSV) * kSlot;
-        if (elect_one()) {
-#pragma unroll
-          for (int k = 0; k < BS / 16; ++k)
-            mma_bf16_ts(d_o, d_s + (gp & 1) * BS + k * 8, b0 + (uint64_t)(((half * 4 + k) * 2048) >> 4),
-                        idPV, (!first || k > 0) ? 1u : 0u);
-          mma_commit(bar(BAR_OD + t));
-          for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_VE + vg % NSV));
-          if (last) mma_commit(bar(BAR_OI + t));
-        }
-        __syncwarp();
-      };
-      uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, g = 0, of_cnt = 0, of_need = 0;
-      bool ok = true;
-      for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
-        const Item it = make_item<CAUSAL>(a, id);
-        const int n_t = (t == 0 ? it.A : it.B).n_tiles;  // key tiles this tile reads
-        const int n_o = (t == 0 ? it.B : it.A).n_tiles;  // key tiles the other tile reads
-        const int n_kv = it.n_kv;
-        // Only an issuer that reads a stage releases it. Where the other tile does not
-        // read stage j (j >= n_o), this issuer brings both arrivals, so a stage is never
-        // handed back to TMA while a product of either tile may still read it.
-        auto rel = [&](int j) { return j < n_o ? 1 : 2; };
-        if (n_t == 0) {  // only B can be missing: A covers the K/V arrivals
-          if (elect_one()) mma_commit(q_empty);  // its Q_B (never read) may be replaced
+        if (!ok && lane == 0) fail(misc, a.err_flag);
+        // Every issued copy must land before the CTA's shared memory is released
+        // (immediate on the normal path, where the MMA warp already waited for them).
+        bool drained = true;
+        if (q_cnt > 0 && (!warp_wait(bar(BAR_Q), (q_cnt - 1) & 1) || !warp_wait(bar(BAR_Q1), (q_cnt - 1) & 1)))
+          drained = false;
+        for (uint32_t s = 0; s < NSK && s < k_cnt; ++s)
+          if (!warp_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) drained = false;
+        for (uint32_t s = 0; s < NSV && s < v_cnt; ++s)
+          if (!warp_wait(bar(BAR_VF + s), ((v_cnt - 1 - s) / NSV) & 1)) drained = false;
+        if (!drained && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      }
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------------ MMA issuers
+      // One thread per query tile (warp 1: A, warp 2: B), so each tile's chain
+      // S -> softmax -> PV runs at its own pace, and tile A moves on to the next item
+      // while B finishes. They share only the K/V stages, whose release barriers take
+      // one arrival from each.
+      {
+        const int t = warp - 1;
+        const uint32_t idS = idesc_bf16_f32(BM, BS, false, false);
+        const uint32_t idPV = idesc_bf16_f32(BM, HD, false, true);
+        // Descriptors are built once; a K step inside a tile only moves the start
+        // address, i.e. adds (byte offset >> 4) to the low field. The largest start
+        // (under 232 KB) plus the largest step stays inside the 14-bit field. Ring slots
+        // and the two Q tiles are TILE bytes apart: slot i's descriptor is the first
+        // slot's plus i * (TILE >> 4).
+        constexpr uint64_t kSlot = TILE >> 4;
+        const uint64_t dq = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B) + (uint64_t)t * kSlot;
+        const uint64_t dk0 = smem_desc(sb + SM_K, 16, 1024, kSwizzle128B);
+        const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
+        const uint32_t d_s = tmem + COL_S + t * BN, d_o = tmem + COL_O + t * HD;
+        const uint32_t q_full = bar(t == 0 ? BAR_Q : BAR_Q1), q_empty = bar(BAR_QE + t);
+        // S for global step gs (keys [64*half, 64*half + 64) of the K tile at ring position
+        // kg) into S buffer gs & 1; then the K stage's release (rel arrivals) after the
+        // tile's second half, and Q_t's release after the item's last step.
+        auto issue_s = [&](uint32_t gs, uint32_t kg, int half, int rel_n, bool q_done) {
+          const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot + (uint64_t)((half * BS * 128) >> 4);
+          if (elect_one()) {
+  #pragma unroll
+            for (int k = 0; k < HD / 16; ++k) {
+              const uint64_t off = (uint64_t)(((k / 4) * SUB + (k % 4) * 32) >> 4);
+              mma_bf16_ss(d_s + (gs & 1) * BS, dq + off, b0 + off, idS, k > 0);
+            }
+            mma_commit(bar(BAR_SF + 2 * t + (gs & 1)));
+            if (q_done) mma_commit(q_empty);  // the last product that reads this Q tile
+            for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_KE + kg % NSK));
+          }
           __syncwarp();
+        };
+        // O_t (+)= P_gp V over keys [64*half, +64) of the V tile at ring position vg; then
+        // o_done, the V stage's release after the tile's second half, o_item after the
+        // item's last step.
+        auto issue_pv = [&](uint32_t gp, uint32_t vg, int half, bool first, int rel_n, bool last) {
+          const uint64_t b0 = dv0 + (uint64_t)(vg % NSV) * kSlot;
+          if (elect_one()) {
+  #pragma unroll
+            for (int k = 0; k < BS / 16; ++k)
+              mma_bf16_ts(d_o, d_s + (gp & 1) * BS + k * 8, b0 + (uint64_t)(((half * 4 + k) * 2048) >> 4),
+                          idPV, (!first || k > 0) ? 1u : 0u);
+            mma_commit(bar(BAR_OD + t));
+            for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_VE + vg % NSV));
+            if (last) mma_commit(bar(BAR_OI + t));
+          }
+          __syncwarp();
+        };
+        uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, g = 0, of_cnt = 0, of_need = 0;
+        bool ok = true;
+        for (int id = blockIdx.x; ok && id < n_items; id += gridDim.x) {
+          const Item it = make_item<CAUSAL>(a, id);
+          const int n_t = (t == 0 ? it.A : it.B).n_tiles;  // key tiles this tile reads
+          const int n_o = (t == 0 ? it.B : it.A).n_tiles;  // key tiles the other tile reads
+          const int n_kv = it.n_kv;
+          // Only an issuer that reads a stage releases it. Where the other tile does not
+          // read stage j (j >= n_o), this issuer brings both arrivals, so a stage is never
+          // handed back to TMA while a product of either tile may still read it.
+          auto rel = [&](int j) { return j < n_o ? 1 : 2; };
+          if (n_t == 0) {  // only B can be missing: A covers the K/V arrivals
+            if (elect_one()) mma_commit(q_empty);  // its Q_B (never read) may be replaced
+            __syncwarp();
+            k_cnt += n_kv;
+            v_cnt += n_kv;
+            ++q_cnt;
+            continue;
+          }
+          const int n_s = 2 * n_t;  // 64-key steps
+          if (!warp_wait(q_full, q_cnt & 1) || !warp_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
+            ok = false;
+            break;
+          }
+          ++q_cnt;
+          tc_fence_after();
+          // S for the first two steps (both halves of K tile 0); the buffers were last read
+          // by the previous item's last two PV products, issued earlier by this thread.
+          issue_s(g, k_cnt, 0, 0, false);
+          issue_s(g + 1, k_cnt, 1, rel(0), n_s == 2);
+          for (int st = 0; st < n_s; ++st, ++g) {
+            const int j = st >> 1, half = st & 1;
+            if (!warp_wait(bar(BAR_PF + 2 * t + (g & 1)), (g >> 1) & 1)) { ok = false; break; }
+            // the previous item's epilogue must have read O before it is overwritten
+            if (st == 0 && of_need > of_cnt) {
+              if (!warp_wait(bar(BAR_OF + t), of_cnt & 1)) { ok = false; break; }
+              ++of_cnt;
+            }
+            const uint32_t vg = v_cnt + j;
+            if (half == 0 && !warp_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(g, vg, half, st == 0, half == 1 ? rel(j) : 0, st == n_s - 1);
+            // S two steps ahead reuses P_g's buffer: the in-order tensor pipe reads P_g first.
+            const int sn = st + 2;
+            if (sn < n_s) {
+              const uint32_t kg = k_cnt + (sn >> 1);
+              if ((sn & 1) == 0 && !warp_wait(bar(BAR_KF + kg % NSK), (kg / NSK) & 1)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(g + 2, kg, sn & 1, (sn & 1) ? rel(sn >> 1) : 0, sn == n_s - 1);
+            }
+          }
           k_cnt += n_kv;
           v_cnt += n_kv;
-          ++q_cnt;
-          continue;
+          ++of_need;
         }
-        const int n_s = 2 * n_t;  // 64-key steps
-        if (!warp_wait(q_full, q_cnt & 1) || !warp_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
-          ok = false;
-          break;
-        }
-        ++q_cnt;
-        tc_fence_after();
-        // S for the first two steps (both halves of K tile 0); the buffers were last read
-        // by the previous item's last two PV products, issued earlier by this thread.
-        issue_s(g, k_cnt, 0, 0, false);
-        issue_s(g + 1, k_cnt, 1, rel(0), n_s == 2);
-        for (int st = 0; st < n_s; ++st, ++g) {
-          const int j = st >> 1, half = st & 1;
-          if (!warp_wait(bar(BAR_PF + 2 * t + (g & 1)), (g >> 1) & 1)) { ok = false; break; }
-          // the previous item's epilogue must have read O before it is overwritten
-          if (st == 0 && of_need > of_cnt) {
-            if (!warp_wait(bar(BAR_OF + t), of_cnt & 1)) { ok = false; break; }
-            ++of_cnt;
-          }
-          const uint32_t vg = v_cnt + j;
-          if (half == 0 && !warp_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(g, vg, half, st == 0, half == 1 ? rel(j) : 0, st == n_s - 1);
-          // S two steps ahead reuses P_g's buffer: the in-order tensor pipe reads P_g first.
-          const int sn = st + 2;
-          if (sn < n_s) {
-            const uint32_t kg = k_cnt + (sn >> 1);
-            if ((sn & 1) == 0 && !warp_wait(bar(BAR_KF + kg % NSK), (kg / NSK) & 1)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(g + 2, kg, sn & 1, (sn & 1) ? rel(sn >> 1) : 0, sn == n_s - 1);
-          }
-        }
-        k_cnt += n_kv;
-        v_cnt += n_kv;
-        ++of_need;
+        if (!ok && lane == 0) fail(misc, a.err_flag);
+        // Every issued product must finish before TMEM is freed.
+        if (elect_one()) mma_commit(bar(BAR_DRAIN + t));
+        __syncwarp();
+        if (!warp_wait(bar(BAR_DRAIN + t), 0) && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
       }
-      if (!ok && lane == 0) fail(misc, a.err_flag);
-      // Every issued product must finish before TMEM is freed.
-      if (elect_one()) mma_commit(bar(BAR_DRAIN + t));
-      __syncwarp();
-      if (!warp_wait(bar(BAR_DRAIN + t), 0) && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
     }
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
