@@ -20,28 +20,29 @@ namespace pkv {
 namespace {
 
 
-// One CTA per (request, query head) row: combines the prefix chunks' and the
-// suffix splits' partial states by log-sum-exp (merge_row_cta).
+// One warp per (request, query head) row, eight rows per CTA: combines the prefix
+// chunks' and the suffix splits' partial states by log-sum-exp (merge_row_warp).
 constexpr int kCascadeMergeWarps = 8;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(const CascadeArgs a) {
-  const int row = blockIdx.x;
+  const int row = blockIdx.x * kCascadeMergeWarps + (threadIdx.x >> 5);
   const int rows = a.n_requests * a.n_qo_heads;
+  if (row >= rows) return;
   const int r = row / a.n_qo_heads;
   const int P = a.page_size;
   const int n_pre = a.prefix_len > 0 ? a.prefix_chunks : 0;
   const int L = __ldg(a.suffix_lens + r);
   T* out = static_cast<T*>(a.out) + (size_t)row * D;
   if (L < 0 || L > a.max_suffix_blocks * P) {  // the decode kernel flagged it
-    for (int d = threadIdx.x; d < D; d += blockDim.x) out[d] = merge_cast<T>(NAN);
-    if (a.lse && threadIdx.x == 0) a.lse[row] = NAN;
+    for (int d = threadIdx.x & 31; d < D; d += 32) out[d] = merge_cast<T>(NAN);
+    if (a.lse && (threadIdx.x & 31) == 0) a.lse[row] = NAN;
     return;
   }
   const int nblk = (L + P - 1) / P;
   const int n_suf = (nblk + a.suffix_pages_per_split - 1) / a.suffix_pages_per_split;
   // partial i < n_pre: prefix chunk i; otherwise suffix split i - n_pre
-  merge_row_cta<T, D, kCascadeMergeWarps>(
+  merge_row_warp<T, D>(
       n_pre + n_suf,
       [&](int i) {
         return i < n_pre ? a.pre_lse[(size_t)i * rows + row]
@@ -162,10 +163,11 @@ int launch_cascade(const CascadeArgs& a, cudaStream_t stream) {
   // 3) merge
   const int rows = a.n_requests * a.n_qo_heads;
   if (a.head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  const int blocks = (rows + kCascadeMergeWarps - 1) / kCascadeMergeWarps;
   if (a.dtype == PKV_BF16)
-    cascade_merge_kernel<__nv_bfloat16, 128><<<rows, kCascadeMergeWarps * 32, 0, stream>>>(a);
+    cascade_merge_kernel<__nv_bfloat16, 128><<<blocks, kCascadeMergeWarps * 32, 0, stream>>>(a);
   else
-    cascade_merge_kernel<float, 128><<<rows, kCascadeMergeWarps * 32, 0, stream>>>(a);
+    cascade_merge_kernel<float, 128><<<blocks, kCascadeMergeWarps * 32, 0, stream>>>(a);
   return check_launch(cudaGetLastError());
 }
 

@@ -5,13 +5,14 @@
 namespace pkv {
 
 // Combines the live splits of each (sequence, query head) row by log-sum-exp
-// (merge_row_cta). Rows whose sequence fits in one split were written by the
-// decode kernel and are skipped here. One CTA of eight warps per row.
+// (merge_row_warp). Rows whose sequence fits in one split were written by the
+// decode kernel and are skipped here. One warp per row, eight rows per CTA.
 constexpr int kMergeWarps = 8;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_splits_kernel(const DecodeArgs a) {
-  const int row = blockIdx.x;
+  const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= a.batch * a.n_qo_heads) return;
   const int b = row / a.n_qo_heads;
   const int P = a.page_size;
   const int L = __ldg(a.kv_lens + b);
@@ -21,7 +22,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_splits_kernel(const De
   if (n_live < 2) return;
   const float* pl = a.part_lse + (size_t)row * a.num_splits;
   const float* po = a.part_o + (size_t)row * a.num_splits * D;
-  merge_row_cta<T, D, kMergeWarps>(
+  merge_row_warp<T, D>(
       n_live, [&](int i) { return pl[i]; }, [&](int i) { return po + (size_t)i * D; },
       static_cast<T*>(a.out) + (size_t)row * D, a.lse ? a.lse + row : nullptr);
 }
@@ -29,7 +30,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_splits_kernel(const De
 template <typename T, int D>
 int launch_merge_t(const DecodeArgs& a, cudaStream_t stream) {
   const int rows = a.batch * a.n_qo_heads;
-  merge_splits_kernel<T, D><<<rows, kMergeWarps * 32, 0, stream>>>(a);
+  merge_splits_kernel<T, D><<<(rows + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, stream>>>(a);
   return check_launch(cudaGetLastError());
 }
 

@@ -1,4 +1,4 @@
-// Log-sum-exp merge of n partial softmax states of one output row, spread over a CTA.
+// Log-sum-exp merge of n partial softmax states of one output row, by one warp.
 //
 // Partial i covers a disjoint set of keys and holds (O_i, lse_i), where O_i is
 // normalised over its keys. With M = max_i lse_i and w_i = exp(lse_i - M):
@@ -6,10 +6,6 @@
 // FlashDecoding computes the partials independently and combines them all at the
 // end ("【FlashAttention-V4，非官方】FlashDecoding++", section 1). No partial
 // (n = 0, or every lse = -inf) gives out = 0 and lse = -inf. A NaN partial gives NaN.
-//
-// Warp w takes partials w, w + NW, ..., and each lane owns D/32 columns; a warp's
-// loads are independent, so they are all in flight at once. The warps then
-// combine through shared memory.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -27,39 +23,53 @@ __device__ __forceinline__ float merge_cast<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 merge_cast<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// DL consecutive floats from a 4*DL-byte aligned address, in one load where DL is 2 or 4.
+template <int DL>
+__device__ __forceinline__ void load_cols(const float* p, float (&x)[DL]) {
+  if constexpr (DL == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+  } else if constexpr (DL == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    x[0] = v.x, x[1] = v.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < DL; ++e) x[e] = p[e];
+  }
+}
+
 // `lse_of(i)` and `o_of(i)` give partial i's lse and a pointer to its D floats
-// (16-byte aligned). Called by all NW*32 threads of the CTA with the same arguments.
-template <typename T, int D, int NW, typename LseF, typename OF>
-__device__ __forceinline__ void merge_row_cta(int n, LseF lse_of, OF o_of, T* out, float* lse_out) {
+// (16-byte aligned); every lane of the warp calls this with the same arguments. Lane l
+// owns columns [l*D/32, (l+1)*D/32). Every lane computes the weights itself (the lse
+// loads are broadcasts), and the partials' loads are issued four at a time before any
+// is used. No shared memory and no CTA barrier, so a CTA can hold one row per warp.
+template <typename T, int D, typename LseF, typename OF>
+__device__ __forceinline__ void merge_row_warp(int n, LseF lse_of, OF o_of, T* out, float* lse_out) {
   constexpr int DL = D / 32;
   constexpr float kL2e = 1.4426950408889634f;
-  __shared__ float s_acc[NW][D];
-  __shared__ float s_l[NW];
   const int lane = threadIdx.x & 31;
-  const int w = threadIdx.x >> 5;
   float M = -INFINITY;
   for (int i = lane; i < n; i += 32) M = fmaxf(M, lse_of(i));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (n == 0 || M == -INFINITY) {  // same on every warp
-    for (int d = threadIdx.x; d < D; d += NW * 32) out[d] = merge_cast<T>(0.0f);
-    if (lse_out && threadIdx.x == 0) *lse_out = -INFINITY;
+  T* o_row = out + lane * DL;
+  if (n == 0 || M == -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < DL; ++e) o_row[e] = merge_cast<T>(0.0f);
+    if (lse_out && lane == 0) *lse_out = -INFINITY;
     return;
   }
   float acc[DL];
 #pragma unroll
   for (int e = 0; e < DL; ++e) acc[e] = 0.0f;
   float l = 0.0f;
-  int i = w;
-  // up to four partials per round, loads issued before any is used
-  for (; i + 3 * NW < n; i += 4 * NW) {
+  int i = 0;
+  for (; i + 3 < n; i += 4) {
     float x[4][DL], wt[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      wt[k] = lse_of(i + k * NW);
-      const float* o = o_of(i + k * NW) + lane * DL;
-#pragma unroll
-      for (int e = 0; e < DL; ++e) x[k][e] = o[e];
+      wt[k] = lse_of(i + k);
+      load_cols<DL>(o_of(i + k) + lane * DL, x[k]);
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -69,28 +79,18 @@ __device__ __forceinline__ void merge_row_cta(int n, LseF lse_of, OF o_of, T* ou
       for (int e = 0; e < DL; ++e) acc[e] = fmaf(wk, x[k][e], acc[e]);
     }
   }
-  for (; i < n; i += NW) {
+  for (; i < n; ++i) {
     const float wk = ex2((lse_of(i) - M) * kL2e);
-    const float* o = o_of(i) + lane * DL;
+    float x[DL];
+    load_cols<DL>(o_of(i) + lane * DL, x);
     l += wk;
 #pragma unroll
-    for (int e = 0; e < DL; ++e) acc[e] = fmaf(wk, o[e], acc[e]);
+    for (int e = 0; e < DL; ++e) acc[e] = fmaf(wk, x[e], acc[e]);
   }
+  const float inv = 1.0f / l;
 #pragma unroll
-  for (int e = 0; e < DL; ++e) s_acc[w][lane * DL + e] = acc[e];
-  if (lane == 0) s_l[w] = l;
-  __syncthreads();
-  float L = 0.0f;
-#pragma unroll
-  for (int k = 0; k < NW; ++k) L += s_l[k];
-  const float inv = 1.0f / L;
-  for (int d = threadIdx.x; d < D; d += NW * 32) {
-    float s = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NW; ++k) s += s_acc[k][d];
-    out[d] = merge_cast<T>(s * inv);
-  }
-  if (lse_out && threadIdx.x == 0) *lse_out = M + logf(L);
+  for (int e = 0; e < DL; ++e) o_row[e] = merge_cast<T>(acc[e] * inv);
+  if (lse_out && lane == 0) *lse_out = M + logf(l);
 }
 
 }  // namespace pkv
