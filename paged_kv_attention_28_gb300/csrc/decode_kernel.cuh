@@ -59,6 +59,9 @@ struct DecodeCfg {
   static constexpr int NSTAGE = 8;                 // ring depth (multiple of NW)
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int MIN_BLOCKS = (G >= 8 || (G == 4 && UNIFIED)) ? 2 : 3;
+  // G >= 4: the row's lanes reduce the G dot products by halving exchanges, after which
+  // each lane holds one head's full score (reduce_scatter_heads).
+  static constexpr bool SCATTER = G >= 4 && G <= LPT;
   static constexpr int BAR_OFF = 2 * NSTAGE * TILE;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NSTAGE * 8;
   static constexpr int SMEM = FLAG_OFF + 16;
@@ -84,6 +87,43 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
+}
+
+// Reduces G per-lane partial dot products over the LPT lanes of a token row so that
+// each lane ends with the full sum of one head: head j / (LPT / G), j = lane % LPT.
+// Stage r exchanges half of the values still held with the lane LPT >> (r + 1) away:
+// the lane with that bit set keeps the upper half of the heads, its partner the lower.
+// After log2 G stages one value is left, summed over the lanes that differ in those
+// bits, and plain xor steps sum it over the remaining ones. That is G - 1 + log2(LPT/G)
+// shuffles per row where reducing every head over every lane takes G * log2 LPT.
+template <int G, int LPT>
+__device__ __forceinline__ float reduce_scatter_heads(const float (&v)[G], int j) {
+  float cur[G];
+#pragma unroll
+  for (int k = 0; k < G; ++k) cur[k] = v[k];
+#pragma unroll
+  for (int half = G / 2, off = LPT / 2; half >= 1; half /= 2, off /= 2) {
+    const bool up = (j & off) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float keep = up ? cur[k + half] : cur[k];
+      const float send = up ? cur[k] : cur[k + half];
+      cur[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float x = cur[0];
+#pragma unroll
+  for (int off = LPT / (2 * G); off >= 1; off /= 2) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// v[h] for a per-lane head index h (selects, no local-memory indexing).
+template <int G>
+__device__ __forceinline__ float pick(const float (&v)[G], int h) {
+  float x = v[0];
+#pragma unroll
+  for (int k = 1; k < G; ++k) x = (h == k) ? v[k] : x;
+  return x;
 }
 
 struct DecodeFlags {
@@ -261,6 +301,10 @@ decode_paged_kernel(const DecodeArgs a) {
     for (int e = 0; e < DP2; ++e) acc2[gi][e] = 0ull;  // (+0, +0)
   }
   int fallbacks = 0;
+  // SCATTER: this lane's head and its running sum (lsum[] is filled after the loop)
+  static_assert(G <= C::LPT, "a token row has at least one lane per head");
+  const int h_own = j / (C::LPT / G);
+  float lsum_own = 0.0f;
 
   if (warp < C::NW) {
     uint64_t q2[G][DP2];
@@ -309,52 +353,120 @@ decode_paged_kernel(const DecodeArgs a) {
             sc[it][gi] = d.x + d.y;
           }
         }
+        if constexpr (C::SCATTER) {
+          // ---- one head per lane: reduce-scatter the dot products, softmax on the lane's
+          // own head, then every head's weight for PV from the lanes that own it
+          constexpr int LPH = C::LPT / G;  // lanes per head within a token row
+          float so[C::NIT];
 #pragma unroll
-        for (int off = 1; off < C::LPT; off <<= 1)
-#pragma unroll
-          for (int it = 0; it < C::NIT; ++it)
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) sc[it][gi] += __shfl_xor_sync(0xffffffffu, sc[it][gi], off);
-#pragma unroll
-        for (int it = 0; it < C::NIT; ++it) {
-          const int t = (ch * C::NIT + it) * C::TPI + tg;
-          if (t >= valid) {
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) sc[it][gi] = -INFINITY;
+          for (int it = 0; it < C::NIT; ++it) {
+            so[it] = reduce_scatter_heads<G, C::LPT>(sc[it], j);
+            const int t = (ch * C::NIT + it) * C::TPI + tg;
+            if (t >= valid) so[it] = -INFINITY;
           }
-        }
-
-        if constexpr (!UNIFIED) {
+          // this chunk's max of head gi, on every lane (lane gi * LPH owns head gi)
+          auto chunk_max = [&](float (&mx)[G]) {
+            float mo = so[0];
 #pragma unroll
-          for (int gi = 0; gi < G; ++gi) {
-            float mx = sc[0][gi];
+            for (int it = 1; it < C::NIT; ++it) mo = fmaxf(mo, so[it]);
 #pragma unroll
-            for (int it = 1; it < C::NIT; ++it) mx = fmaxf(mx, sc[it][gi]);
+            for (int off = C::LPT; off < 32; off <<= 1) mo = fmaxf(mo, __shfl_xor_sync(0xffffffffu, mo, off));
 #pragma unroll
-            for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            if (mx > ref[gi]) {  // warp-uniform: every lane holds the same mx and ref
-              const float alpha = ex2(ref[gi] - mx);
-              const uint64_t al2 = pk2(alpha, alpha);
-              ref[gi] = mx;
-              lsum[gi] *= alpha;
+            for (int gi = 0; gi < G; ++gi) mx[gi] = __shfl_sync(0xffffffffu, mo, gi * LPH);
+          };
+          auto rescale = [&](int gi, float alpha) {
+            const uint64_t al2 = pk2(alpha, alpha);
+            if (h_own == gi) lsum_own *= alpha;
 #pragma unroll
-              for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(acc2[gi][e], al2, 0ull);
+            for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(acc2[gi][e], al2, 0ull);
+          };
+          if constexpr (!UNIFIED) {
+            float mx[G];
+            chunk_max(mx);
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              if (mx[gi] > ref[gi]) {  // warp-uniform
+                rescale(gi, ex2(ref[gi] - mx[gi]));
+                ref[gi] = mx[gi];
+              }
+            }
+          } else {
+            const float ref_o = pick<G>(ref, h_own);
+            bool viol = false, all_low = true;
+#pragma unroll
+            for (int it = 0; it < C::NIT; ++it) {
+              viol |= so[it] > ref_o + beta2;
+              all_low &= so[it] < ref_o - beta2;
+            }
+            if (first_chunk) {
+              // a head underflows when every lane that owns it saw only low logits
+              const unsigned low = __ballot_sync(0xffffffffu, all_low);
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) {
+                unsigned hm = 0;
+#pragma unroll
+                for (int r = 0; r < 32 / C::LPT; ++r) hm |= ((1u << LPH) - 1u) << (r * C::LPT + gi * LPH);
+                viol |= (low & hm) == hm;
+              }
+            }
+            if (__any_sync(0xffffffffu, viol)) {
+              float mx[G];
+              chunk_max(mx);
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) {
+                const bool hi = mx[gi] > ref[gi] + beta2;
+                const bool lo = first_chunk && mx[gi] < ref[gi] - beta2;
+                if (hi) rescale(gi, ex2(ref[gi] - mx[gi]));
+                if (hi || lo) {
+                  ref[gi] = mx[gi];
+                  ++fallbacks;
+                }
+              }
+            }
+            first_chunk = false;
+          }
+          const float ref_o = pick<G>(ref, h_own);
+#pragma unroll
+          for (int it = 0; it < C::NIT; ++it) {
+            so[it] = ex2(so[it] - ref_o);
+            lsum_own += so[it];
+          }
+#pragma unroll
+          for (int it = 0; it < C::NIT; ++it) {
+            const int t = (ch * C::NIT + it) * C::TPI + tg;
+            float pw[G];
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) pw[gi] = __shfl_sync(0xffffffffu, so[it], tg * C::LPT + gi * LPH);
+            uint64_t v2[DP2];
+#pragma unroll
+            for (int c = 0; c < C::NV; ++c)
+              load_row_pairs<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+            if (t < valid) {
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) {
+                const uint64_t p2 = pk2(pw[gi], pw[gi]);
+#pragma unroll
+                for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+              }
             }
           }
         } else {
-          bool viol = false;
 #pragma unroll
-          for (int gi = 0; gi < G; ++gi) {
-            bool all_low = true;
+          for (int off = 1; off < C::LPT; off <<= 1)
 #pragma unroll
-            for (int it = 0; it < C::NIT; ++it) {
-              viol |= sc[it][gi] > ref[gi] + beta2;
-              all_low &= sc[it][gi] < ref[gi] - beta2;
+            for (int it = 0; it < C::NIT; ++it)
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) sc[it][gi] += __shfl_xor_sync(0xffffffffu, sc[it][gi], off);
+#pragma unroll
+          for (int it = 0; it < C::NIT; ++it) {
+            const int t = (ch * C::NIT + it) * C::TPI + tg;
+            if (t >= valid) {
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) sc[it][gi] = -INFINITY;
             }
-            if (first_chunk) viol |= __all_sync(0xffffffffu, all_low);
           }
-          if (__any_sync(0xffffffffu, viol)) {
-            // Fallback: move each head's reference to this chunk's max where needed.
+
+          if constexpr (!UNIFIED) {
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
               float mx = sc[0][gi];
@@ -362,47 +474,78 @@ decode_paged_kernel(const DecodeArgs a) {
               for (int it = 1; it < C::NIT; ++it) mx = fmaxf(mx, sc[it][gi]);
 #pragma unroll
               for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-              const bool hi = mx > ref[gi] + beta2;
-              const bool lo = first_chunk && mx < ref[gi] - beta2;
-              if (hi) {
-                // Raise the reference and shrink what was accumulated against the old one.
+              if (mx > ref[gi]) {  // warp-uniform: every lane holds the same mx and ref
                 const float alpha = ex2(ref[gi] - mx);
                 const uint64_t al2 = pk2(alpha, alpha);
+                ref[gi] = mx;
                 lsum[gi] *= alpha;
 #pragma unroll
                 for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(acc2[gi][e], al2, 0ull);
               }
-              if (hi || lo) {
-                // A lowered reference (first chunk only) has nothing accumulated to rescale;
-                // ex2(old - new) would overflow there.
-                ref[gi] = mx;
-                ++fallbacks;
-              }
             }
-          }
-          first_chunk = false;
-        }
-
-#pragma unroll
-        for (int it = 0; it < C::NIT; ++it)
-#pragma unroll
-          for (int gi = 0; gi < G; ++gi) {
-            sc[it][gi] = ex2(sc[it][gi] - ref[gi]);
-            lsum[gi] += sc[it][gi];
-          }
-#pragma unroll
-        for (int it = 0; it < C::NIT; ++it) {
-          const int t = (ch * C::NIT + it) * C::TPI + tg;
-          uint64_t v2[DP2];
-#pragma unroll
-          for (int c = 0; c < C::NV; ++c)
-            load_row_pairs<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
-          if (t < valid) {
+          } else {
+            bool viol = false;
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) {
-              const uint64_t p2 = pk2(sc[it][gi], sc[it][gi]);
+              bool all_low = true;
 #pragma unroll
-              for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+              for (int it = 0; it < C::NIT; ++it) {
+                viol |= sc[it][gi] > ref[gi] + beta2;
+                all_low &= sc[it][gi] < ref[gi] - beta2;
+              }
+              if (first_chunk) viol |= __all_sync(0xffffffffu, all_low);
+            }
+            if (__any_sync(0xffffffffu, viol)) {
+              // Fallback: move each head's reference to this chunk's max where needed.
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) {
+                float mx = sc[0][gi];
+#pragma unroll
+                for (int it = 1; it < C::NIT; ++it) mx = fmaxf(mx, sc[it][gi]);
+#pragma unroll
+                for (int off = C::LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const bool hi = mx > ref[gi] + beta2;
+                const bool lo = first_chunk && mx < ref[gi] - beta2;
+                if (hi) {
+                  // Raise the reference and shrink what was accumulated against the old one.
+                  const float alpha = ex2(ref[gi] - mx);
+                  const uint64_t al2 = pk2(alpha, alpha);
+                  lsum[gi] *= alpha;
+#pragma unroll
+                  for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(acc2[gi][e], al2, 0ull);
+                }
+                if (hi || lo) {
+                  // A lowered reference (first chunk only) has nothing accumulated to rescale;
+                  // ex2(old - new) would overflow there.
+                  ref[gi] = mx;
+                  ++fallbacks;
+                }
+              }
+            }
+            first_chunk = false;
+          }
+
+#pragma unroll
+          for (int it = 0; it < C::NIT; ++it)
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+              sc[it][gi] = ex2(sc[it][gi] - ref[gi]);
+              lsum[gi] += sc[it][gi];
+            }
+#pragma unroll
+          for (int it = 0; it < C::NIT; ++it) {
+            const int t = (ch * C::NIT + it) * C::TPI + tg;
+            uint64_t v2[DP2];
+#pragma unroll
+            for (int c = 0; c < C::NV; ++c)
+              load_row_pairs<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+            if (t < valid) {
+#pragma unroll
+              for (int gi = 0; gi < G; ++gi) {
+                const uint64_t p2 = pk2(sc[it][gi], sc[it][gi]);
+#pragma unroll
+                for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+              }
             }
           }
         }
@@ -411,12 +554,18 @@ decode_paged_kernel(const DecodeArgs a) {
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
 
+    if constexpr (C::SCATTER) {
+#pragma unroll
+      for (int off = C::LPT; off < 32; off <<= 1) lsum_own += __shfl_xor_sync(0xffffffffu, lsum_own, off);
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) lsum[gi] = __shfl_sync(0xffffffffu, lsum_own, gi * (C::LPT / G));
+    }
     // Sum the per-row partials over the token rows of the warp (lanes with equal j).
 #pragma unroll
     for (int off = C::LPT; off < 32; off <<= 1)
 #pragma unroll
       for (int gi = 0; gi < G; ++gi) {
-        lsum[gi] += __shfl_xor_sync(0xffffffffu, lsum[gi], off);
+        if constexpr (!C::SCATTER) lsum[gi] += __shfl_xor_sync(0xffffffffu, lsum[gi], off);
 #pragma unroll
         for (int e = 0; e < DP2; ++e) {
           float2 v = upk2(acc2[gi][e]);
