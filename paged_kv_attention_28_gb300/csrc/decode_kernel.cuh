@@ -40,12 +40,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kUnifiedBeta = 60.0f;
 
 // Lanes per token row: 16 halves the registers a lane holds for G >= 4 (q and the
-// accumulators of G heads), so that G = 4 fits three CTAs per SM; the unified-max
-// variant of G = 4 measured faster with 8 lanes and two CTAs per SM.
+// accumulators of G heads), so that G = 4 fits three CTAs per SM, the online and the
+// unified-max variant alike (with the reduce-scatter below, 8 lanes and two CTAs per SM
+// measured 5 % slower on the unified-max variant and 5 % slower on the online one).
 template <typename T, int D, int P, int G, bool UNIFIED = false>
 struct DecodeCfg {
   static constexpr int ES = sizeof(T);
-  static constexpr int LPT = (G >= 8 || (G == 4 && !UNIFIED)) ? 16 : 8;
+  static constexpr int LPT = (G >= 4) ? 16 : 8;
   static constexpr int TPI = 32 / LPT;             // token rows a warp covers per step
   static constexpr int DPL = D / LPT;              // head dims held per lane
   static constexpr int VEC = (16 / ES < DPL) ? 16 / ES : DPL;  // elements per smem load
@@ -58,7 +59,7 @@ struct DecodeCfg {
   static constexpr int NW = 4;                     // consumer warps
   static constexpr int NSTAGE = 8;                 // ring depth (multiple of NW)
   static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int MIN_BLOCKS = (G >= 8 || (G == 4 && UNIFIED)) ? 2 : 3;
+  static constexpr int MIN_BLOCKS = (G >= 8) ? 2 : 3;
   // G >= 4: the row's lanes reduce the G dot products by halving exchanges, after which
   // each lane holds one head's full score (reduce_scatter_heads).
   static constexpr bool SCATTER = G >= 4 && G <= LPT;
