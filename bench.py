@@ -532,7 +532,9 @@ def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, 
             "ms_per_step": 1000 * t / args.steps, "causal_flops_per_step": flops,
             "roofline": {"bound": "tensor", "achieved": per, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": per / bf16_peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                         "traffic": None, "kernel": "prefill_causal_kernel"},
+                         "traffic": profiled_traffic("causal_prefill_llama7b",
+                                                     source_hash("prefill.cu", "tcgen05.cuh", "ptx.cuh"), 1),
+                         "kernel": "attn_tile_kernel<causal>"},
             "launches": args.steps}
 
 

@@ -41,8 +41,8 @@ __device__ __forceinline__ void load_cols(const float* p, float (&x)[DL]) {
 // `lse_of(i)` and `o_of(i)` give partial i's lse and a pointer to its D floats
 // (16-byte aligned); every lane of the warp calls this with the same arguments. Lane l
 // owns columns [l*D/32, (l+1)*D/32). Every lane computes the weights itself (the lse
-// loads are broadcasts), and the partials' loads are issued four at a time before any
-// is used. No shared memory and no CTA barrier, so a CTA can hold one row per warp.
+// loads are broadcasts), and the partials' loads are issued eight (then four) at a time
+// before any is used. No shared memory and no CTA barrier, so a CTA can hold one row per warp.
 template <typename T, int D, typename LseF, typename OF>
 __device__ __forceinline__ void merge_row_warp(int n, LseF lse_of, OF o_of, T* out, float* lse_out) {
   constexpr int DL = D / 32;
@@ -64,6 +64,21 @@ __device__ __forceinline__ void merge_row_warp(int n, LseF lse_of, OF o_of, T* o
   for (int e = 0; e < DL; ++e) acc[e] = 0.0f;
   float l = 0.0f;
   int i = 0;
+  for (; i + 7 < n; i += 8) {
+    float x[8][DL], wt[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      wt[k] = lse_of(i + k);
+      load_cols<DL>(o_of(i + k) + lane * DL, x[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float wk = ex2((wt[k] - M) * kL2e);
+      l += wk;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) acc[e] = fmaf(wk, x[k][e], acc[e]);
+    }
+  }
   for (; i + 3 < n; i += 4) {
     float x[4][DL], wt[4];
 #pragma unroll
