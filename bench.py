@@ -497,6 +497,29 @@ def other_workloads(B, workloads, dev, stream, steps, hbm_peak):
     ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale), steps, stream, dev)
     entry("single_seq_decode_f32", c.kv_bytes(), ms,
           {"note": "1 MiB of K/V: launch-latency bound; L2 flushed before each call"})
+    # The same call captured once into a CUDA graph and replayed: the library never
+    # allocates, copies to the host or synchronises, so the decode and its split merge
+    # replay as one graph launch on the current buffers.
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
+                                                   c.head_dim, c.page_size, 0, B.PKV_F32), dev)
+
+    def call():
+        B.decode_paged(q, kp, vp, bt, ln, c.scale, out=out, lse=lse, workspace=ws)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    ms = time_calls(graph.replay, steps, stream, dev)
+    entry("single_seq_decode_f32_graph", c.kv_bytes(), ms,
+          {"note": "the same call replayed from a CUDA graph captured once; L2 flushed before each replay"})
     return res
 
 
