@@ -460,6 +460,25 @@ def other_workloads(B, workloads, dev, stream, steps, hbm_peak):
             d.update(extra)
         res[name] = d
 
+    # The Llama-7B batch (same lengths, same page order) over FP8 E4M3 page pools with
+    # per-(page, KV head) scales: half the K/V bytes of the bf16 headline.
+    c = workloads.llama7b_batched_decode_fp8(poison=False)
+    q, kc, vc, ks, vs, bt, ln = (t.to(dev) for t in (c.q, c.k_codes, c.v_codes, c.k_scale,
+                                                     c.v_scale, c.block_table, c.kv_lens))
+    out = torch.empty_like(q)
+    lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
+    S = B.decode_num_splits(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads, c.head_dim,
+                            c.page_size, 0, B.PKV_FP8_E4M3)
+    ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
+                                                   c.head_dim, c.page_size, 0, B.PKV_FP8_E4M3), dev)
+    ms = time_calls(lambda: B.decode_paged_fp8(q, kc, vc, ks, vs, bt, ln, c.scale, out=out, lse=lse,
+                                               workspace=ws), steps, stream, dev)
+    toks = int(c.kv_lens.sum())
+    entry("llama7b_batched_decode_fp8", c.kv_bytes(), ms,
+          {"num_splits": S, "tokens_per_s": toks / (ms / 1e3),
+           "bytes_note": "E4M3 codes of every token's K and V plus the scales of the pages read"})
+    del q, kc, vc, ks, vs, bt, ln, ws
+
     c = workloads.long_context_gqa_decode(poison=False)
     q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
     out = torch.empty_like(q)

@@ -58,6 +58,7 @@ extern "C" {
 /* element types */
 #define PKV_F32 0
 #define PKV_BF16 1
+#define PKV_FP8_E4M3 2 /* page pools of attn_decode_paged_fp8 (planning and workspace queries) */
 
 /* status codes */
 #define PKV_OK 0
@@ -193,6 +194,30 @@ int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void
                                   float scale, int num_splits, int dtype, float phi,
                                   int32_t* fallback_count, void* workspace,
                                   size_t workspace_bytes, int32_t* err_flag, void* stream);
+
+/*
+ * Decode over FP8 page pools. FP8 cuts attention's memory traffic ("TensorRT-LLM
+ * 深度优化：利用FMHA（Fused Multi-Head Attention）内核加速Hopper架构推理", section 4);
+ * the page names neither a format nor a scaling, and this library's reading is:
+ *   - k_pages, v_pages hold E4M3 codes (the OCP 8-bit floating-point format: bias 7,
+ *     3 mantissa bits, no infinities), one byte per element, in the paged layout;
+ *   - k_scale, v_scale : fp32 [num_pages][n_kv_heads], one scale per (page, KV head)
+ *     tile; an element's value is e4m3(code) * scale;
+ *   - q and out are bf16 (dtype PKV_BF16 implied); lse, workspace, splits and
+ *     err_flag are as for attn_decode_paged, with the workspace size from
+ *     attn_decode_workspace_size(..., PKV_FP8_E4M3).
+ * The result is the attention of attn_decode_paged over the dequantised values, with
+ * the per-tile scales applied to the dot products and to the softmax weights. Pools
+ * must be 16-byte aligned. Built for head_dim 64 and 128, page_size 16 and GQA
+ * groups 1, 2, 4 and 8; other shapes return PKV_ERR_UNSUPPORTED.
+ */
+int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
+                          const float* k_scale, const float* v_scale, const int32_t* block_table,
+                          const int32_t* kv_lens, void* out, float* lse, int batch,
+                          int max_blocks_per_seq, int num_pages, int n_qo_heads, int n_kv_heads,
+                          int head_dim, int page_size, float scale, int num_splits,
+                          void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                          void* stream);
 
 /*
  * Merge two partial softmax states over disjoint key sets into one

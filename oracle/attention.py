@@ -23,6 +23,9 @@ multiplies by V. There is no tiling, fusion or reordering beyond that. Sources:
   and updates them all at the end).
 * The unified maximum value: the same page, sections 1 and 3. Partials are
   computed against one shared preset maximum and need no synchronised update.
+* FP8 K/V: "TensorRT-LLM深度优化：利用FMHA（Fused Multi-Head Attention）内核加速
+  Hopper架构推理", section 4 (FP8 lowers the memory traffic). The page names no
+  format and no scaling.
 
 Readings where the pages are silent (the design document lists them too):
 
@@ -35,6 +38,10 @@ Readings where the pages are silent (the design document lists them too):
   Split ``s`` holds blocks ``[s*pps, (s+1)*pps)``.
 * The unified-max partial of a chunk is ``(sum exp(s - phi) v, sum exp(s - phi))``
   with a preset ``phi``. Chunks that share ``phi`` merge by plain sums.
+* FP8 pages hold E4M3 codes (the OCP 8-bit floating-point format), and each
+  (page, KV head) tile of K and of V has one float scale: the element's value is
+  ``e4m3(code) * scale``. Attention over FP8 pages is the plain attention over
+  those values.
 """
 from __future__ import annotations
 
@@ -46,6 +53,7 @@ __all__ = [
     "attend", "gather_sequence", "decode_paged", "prefill_causal", "merge_states",
     "merge_many", "split_ranges", "decode_split_partials", "cascade_decode",
     "unified_max_partials", "unified_max_combine", "unified_max_needs_fallback",
+    "e4m3_to_float", "decode_paged_fp8",
 ]
 
 NEG_INF = -math.inf
@@ -128,6 +136,60 @@ def decode_paged(q, k_pages, v_pages, block_table, kv_lens, scale, rows=None):
             if not heads:
                 continue
             K, V = _gather_fast(k_pages, v_pages, block_table[b], kv_lens[b], g)
+            o, l = attend(q[b, heads], K, V, scale)
+            out[b, heads] = o
+            lse[b, heads] = l
+    return out, lse
+
+
+def e4m3_to_float(codes):
+    """Values of FP8 E4M3 codes (any integer array of bytes) as float64.
+
+    The OCP 8-bit floating-point E4M3 format: a sign bit s, four exponent bits e with
+    bias 7 and three mantissa bits m. e = 0 is subnormal, (-1)^s * 2^-6 * m/8. Otherwise
+    the value is (-1)^s * 2^(e-7) * (1 + m/8), except e = 15 with m = 7, which is NaN:
+    the format has no infinities, and its largest finite magnitude is 2^8 * 1.75 = 448.
+    """
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    s = (c >> 7) & 1
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    val = np.where(s == 1, -mag, mag)
+    return np.where((e == 15) & (c & 7 == 7), np.nan, val)
+
+
+def decode_paged_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, kv_lens, scale,
+                     rows=None):
+    """Single-token decode over a paged cache of FP8 E4M3 codes.
+
+    ``k_codes``/``v_codes`` ``[num_pages, Hkv, P, D]`` (bytes), ``k_scale``/``v_scale``
+    ``[num_pages, Hkv]``. Each sequence's tokens are gathered through the block table
+    as in ``decode_paged`` and dequantised (code value times its tile's scale) before
+    the plain attention. Returns ``out[B, Hq, D]`` and ``lse[B, Hq]``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Hq, D = q.shape
+    Hkv = k_codes.shape[1]
+    P = k_codes.shape[2]
+    G = Hq // Hkv
+    ks = np.asarray(k_scale, dtype=np.float64)
+    vs = np.asarray(v_scale, dtype=np.float64)
+    out = np.full((B, Hq, D), np.nan)
+    lse = np.full((B, Hq), np.nan)
+    wanted = None if rows is None else {(int(b), int(h)) for b, h in rows}
+    for b in range(B):
+        t = np.arange(int(kv_lens[b]))
+        pages = None
+        for g in range(Hkv):
+            heads = [h for h in range(g * G, (g + 1) * G)
+                     if wanted is None or (b, h) in wanted]
+            if not heads:
+                continue
+            if pages is None:
+                pages = np.asarray(block_table[b], dtype=np.int64)[t // P]
+            K = e4m3_to_float(k_codes[pages, g, t % P]) * ks[pages, g][:, None]
+            V = e4m3_to_float(v_codes[pages, g, t % P]) * vs[pages, g][:, None]
             o, l = attend(q[b, heads], K, V, scale)
             out[b, heads] = o
             lse[b, heads] = l

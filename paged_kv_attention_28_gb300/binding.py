@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libpkvattn.so")
 
 PKV_F32 = 0
 PKV_BF16 = 1
+PKV_FP8_E4M3 = 2
 PKV_OK = 0
 PKV_ERR_INVALID_ARG = -1
 PKV_ERR_UNSUPPORTED = -2
@@ -32,7 +33,7 @@ EXPORTS = [
     "attn_status_string", "attn_last_cuda_error_string", "attn_decode_num_splits", "attn_decode_workspace_size",
     "attn_decode_paged", "attn_decode_paged_unified_max", "attn_merge_states",
     "attn_prefill_causal", "attn_cascade_workspace_size", "attn_decode_cascade",
-    "attn_decode_paged_noalloc",
+    "attn_decode_paged_noalloc", "attn_decode_paged_fp8",
 ]
 
 
@@ -67,6 +68,8 @@ def _load() -> ctypes.CDLL:
                                                   [f32, i32, i32, f32, vp, vp, sz, vp, vp])
     lib.attn_decode_paged_noalloc.restype = i32
     lib.attn_decode_paged_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [i32] * 7 + [f32, i32, i32, vp, vp]
+    lib.attn_decode_paged_fp8.restype = i32
+    lib.attn_decode_paged_fp8.argtypes = [vp] * 9 + [i32] * 7 + [f32, i32, vp, sz, vp, vp]
     lib.attn_merge_states.restype = i32
     lib.attn_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]
     lib.attn_prefill_causal.restype = i32
@@ -176,6 +179,40 @@ def decode_paged(q, k_pages, v_pages, block_table, kv_lens, scale, num_splits=0,
         st = lib.attn_decode_paged_unified_max(*args, float(unified_phi), _ptr(fallback_count),
                                                _ptr(workspace), wsz, _ptr(err_flag), _stream(stream))
         _check(st, "attn_decode_paged_unified_max")
+    return out, lse
+
+
+def decode_paged_fp8(q, k_codes, v_codes, k_scale, v_scale, block_table, kv_lens, scale,
+                     num_splits=0, out=None, lse=None, workspace=None, err_flag=None, stream=None):
+    """Paged decode over FP8 E4M3 pools through ``attn_decode_paged_fp8``.
+
+    ``q`` bf16 ``[B, Hq, D]``; ``k_codes``/``v_codes`` uint8 ``[num_pages, Hkv, P, D]``;
+    ``k_scale``/``v_scale`` float32 ``[num_pages, Hkv]``. Returns ``(out, lse)``."""
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_codes.shape
+    assert D2 == D
+    max_blocks = block_table.shape[1]
+    _need(q, "q", torch.bfloat16)
+    _need(k_codes, "k_codes", torch.uint8)
+    _need(v_codes, "v_codes", torch.uint8, k_codes.shape)
+    _need(k_scale, "k_scale", torch.float32, (num_pages, Hkv))
+    _need(v_scale, "v_scale", torch.float32, (num_pages, Hkv))
+    _need(block_table, "block_table", torch.int32, (B, max_blocks))
+    _need(kv_lens, "kv_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    ws_bytes = decode_workspace_size(B, max_blocks, Hq, Hkv, D, P, num_splits, PKV_FP8_E4M3)
+    if workspace is None:
+        workspace = alloc_workspace(ws_bytes, q.device)
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.attn_decode_paged_fp8(_ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                   _ptr(v_scale), _ptr(block_table), _ptr(kv_lens), _ptr(out),
+                                   _ptr(lse), B, max_blocks, num_pages, Hq, Hkv, D, P, float(scale),
+                                   int(num_splits), _ptr(workspace), wsz, _ptr(err_flag),
+                                   _stream(stream))
+    _check(st, "attn_decode_paged_fp8")
     return out, lse
 
 

@@ -78,9 +78,13 @@ struct DecodeCall {
   size_t workspace_bytes;
   int32_t* err_flag;
   cudaStream_t stream;
+  // FP8 page pools (dtype is then PKV_BF16, the type of q and out)
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
 };
 
-static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* fallback_count) {
+static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* fallback_count,
+                         bool fp8 = false) {
   if (c.batch < 0 || c.max_blocks < 1 || c.num_pages < 1 || c.n_qo_heads < 1 ||
       c.n_kv_heads < 1 || c.head_dim < 1 || c.page_size < 1 || c.num_splits < 0)
     return PKV_ERR_INVALID_ARG;
@@ -91,12 +95,13 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   if (c.batch == 0) return PKV_OK;
   if (!c.q || !c.k_pages || !c.v_pages || !c.block_table || !c.kv_lens || !c.out)
     return PKV_ERR_INVALID_ARG;
+  if (fp8 && (!c.k_scale || !c.v_scale)) return PKV_ERR_INVALID_ARG;
   if (!aligned16(c.k_pages) || !aligned16(c.v_pages)) return PKV_ERR_INVALID_ARG;
   const int G = c.n_qo_heads / c.n_kv_heads;
   if (!decode_supported(c.dtype, c.head_dim, c.page_size, G)) return PKV_ERR_UNSUPPORTED;
   if (c.batch > 65535 || c.n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, c.n_kv_heads, c.num_splits,
-                                            decode_ctas_per_sm(c.dtype, c.head_dim, G));
+                                            decode_ctas_per_sm(fp8 ? PKV_FP8_E4M3 : c.dtype, c.head_dim, G));
   const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.head_dim, plan.num_splits);
   if (need > 0 && (!c.workspace || c.workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(c.workspace) & 255u) != 0))
@@ -133,6 +138,9 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   a.unified = unified;
   a.phi = phi;
   a.fallback_count = fallback_count;
+  a.fp8 = fp8;
+  a.k_scale = c.k_scale;
+  a.v_scale = c.v_scale;
   return launch_decode(a, c.stream);
 }
 
@@ -163,7 +171,7 @@ int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, in
   if (batch < 0 || max_blocks_per_seq < 1 || n_qo_heads < 1 || n_kv_heads < 1 ||
       head_dim < 1 || page_size < 1 || num_splits < 0 || n_qo_heads % n_kv_heads)
     return PKV_ERR_INVALID_ARG;
-  if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
   return plan_decode_splits(batch, max_blocks_per_seq, n_kv_heads, num_splits,
                             decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads))
       .num_splits;
@@ -201,6 +209,20 @@ int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void
                num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, dtype,
                workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream)};
   return decode_common(c, true, phi, fallback_count);
+}
+
+int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
+                          const float* k_scale, const float* v_scale, const int32_t* block_table,
+                          const int32_t* kv_lens, void* out, float* lse, int batch,
+                          int max_blocks_per_seq, int num_pages, int n_qo_heads, int n_kv_heads,
+                          int head_dim, int page_size, float scale, int num_splits,
+                          void* workspace, size_t workspace_bytes, int32_t* err_flag,
+                          void* stream) {
+  DecodeCall c{q, k_pages, v_pages, block_table, kv_lens, out, lse, batch, max_blocks_per_seq,
+               num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, PKV_BF16,
+               workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream), k_scale,
+               v_scale};
+  return decode_common(c, false, 0.0f, nullptr, true);
 }
 
 int attn_merge_states(const float* out_a, const float* lse_a, const float* out_b,

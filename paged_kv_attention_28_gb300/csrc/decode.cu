@@ -46,24 +46,27 @@ int launch_merge_splits(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 int dispatch_decode_unified(const DecodeArgs& a, cudaStream_t stream);  // decode_um.cu
+int dispatch_decode_fp8(const DecodeArgs& a, cudaStream_t stream);      // decode_fp8.cu
 
 int decode_ctas_per_sm(int dtype, int head_dim, int group) {
-#define PKV_CPS(TT)                                                            \
+#define PKV_CPS(TT, F8)                                                        \
   if (head_dim == 64) {                                                        \
-    if (group == 1) return ctas_per_sm_t<TT, 64, 1>();                         \
-    if (group == 2) return ctas_per_sm_t<TT, 64, 2>();                         \
-    if (group == 4) return ctas_per_sm_t<TT, 64, 4>();                         \
-    if (group == 8) return ctas_per_sm_t<TT, 64, 8>();                         \
+    if (group == 1) return ctas_per_sm_t<TT, 64, 1, F8>();                     \
+    if (group == 2) return ctas_per_sm_t<TT, 64, 2, F8>();                     \
+    if (group == 4) return ctas_per_sm_t<TT, 64, 4, F8>();                     \
+    if (group == 8) return ctas_per_sm_t<TT, 64, 8, F8>();                     \
   } else {                                                                     \
-    if (group == 1) return ctas_per_sm_t<TT, 128, 1>();                        \
-    if (group == 2) return ctas_per_sm_t<TT, 128, 2>();                        \
-    if (group == 4) return ctas_per_sm_t<TT, 128, 4>();                        \
-    if (group == 8) return ctas_per_sm_t<TT, 128, 8>();                        \
+    if (group == 1) return ctas_per_sm_t<TT, 128, 1, F8>();                    \
+    if (group == 2) return ctas_per_sm_t<TT, 128, 2, F8>();                    \
+    if (group == 4) return ctas_per_sm_t<TT, 128, 4, F8>();                    \
+    if (group == 8) return ctas_per_sm_t<TT, 128, 8, F8>();                    \
   }
   if (dtype == PKV_F32) {
-    PKV_CPS(float)
+    PKV_CPS(float, false)
+  } else if (dtype == PKV_FP8_E4M3) {
+    PKV_CPS(__nv_bfloat16, true)
   } else {
-    PKV_CPS(__nv_bfloat16)
+    PKV_CPS(__nv_bfloat16, false)
   }
 #undef PKV_CPS
   return 2;
@@ -79,7 +82,9 @@ int launch_decode_partials(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  const int rc = a.unified ? dispatch_decode_unified(a, stream) : dispatch_decode<false>(a, stream);
+  const int rc = a.fp8       ? dispatch_decode_fp8(a, stream)
+                 : a.unified ? dispatch_decode_unified(a, stream)
+                             : dispatch_decode<false>(a, stream);
   if (rc != PKV_OK) return rc;
   if (a.num_splits > 1) return launch_merge_splits(a, stream);
   return PKV_OK;

@@ -25,8 +25,11 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -43,9 +46,14 @@ constexpr float kUnifiedBeta = 60.0f;
 // accumulators of G heads), so that G = 4 fits three CTAs per SM, the online and the
 // unified-max variant alike (with the reduce-scatter below, 8 lanes and two CTAs per SM
 // measured 5 % slower on the unified-max variant and 5 % slower on the online one).
-template <typename T, int D, int P, int G, bool UNIFIED = false>
+// FP8: the page pools hold E4M3 codes with one float scale per (page, KV head) tile of K
+// and of V; q and the output stay T (bf16). A stage then carries half the bytes and the
+// CTA half the shared memory, and the work per page is what limits a CTA (the same
+// tokens as bf16 took as long with a ring twice as deep), so G = 1 runs five CTAs per SM.
+template <typename T, int D, int P, int G, bool UNIFIED = false, bool FP8 = false>
 struct DecodeCfg {
-  static constexpr int ES = sizeof(T);
+  using KV = std::conditional_t<FP8, uint8_t, T>;  // element type of the page pools
+  static constexpr int ES = sizeof(KV);
   static constexpr int LPT = (G >= 4) ? 16 : 8;
   static constexpr int TPI = 32 / LPT;             // token rows a warp covers per step
   static constexpr int DPL = D / LPT;              // head dims held per lane
@@ -59,13 +67,14 @@ struct DecodeCfg {
   static constexpr int NW = 4;                     // consumer warps
   static constexpr int NSTAGE = 8;                 // ring depth (multiple of NW)
   static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int MIN_BLOCKS = (G >= 8) ? 2 : 3;
+  static constexpr int MIN_BLOCKS = G >= 8 ? 2 : (FP8 && G == 1 ? 5 : 3);
   // G >= 4: the row's lanes reduce the G dot products by halving exchanges, after which
   // each lane holds one head's full score (reduce_scatter_heads).
   static constexpr bool SCATTER = G >= 4 && G <= LPT;
   static constexpr int BAR_OFF = 2 * NSTAGE * TILE;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NSTAGE * 8;
-  static constexpr int SMEM = FLAG_OFF + 16;
+  static constexpr int SCALE_OFF = FLAG_OFF + 16;  // FP8: (k_scale, v_scale) of each stage
+  static constexpr int SMEM = SCALE_OFF + (FP8 ? NSTAGE * 8 : 0);
   static_assert(D % LPT == 0 && DPL % VEC == 0 && VEC % 2 == 0, "head_dim split");
   static_assert(P % TPI == 0 && ITERS % NIT == 0, "page split");
   static_assert(NSTAGE % NW == 0, "stage ownership");
@@ -137,6 +146,61 @@ struct DecodeFlags {
 // Loads VEC elements of one K or V row from shared memory (VEC * sizeof(T)
 // bytes, aligned) as VEC/2 packed (even, odd) fp32 pairs. bf16 -> fp32 is a
 // 16-bit left shift of the bit pattern.
+// FP8 rows stay in f16: two E4M3 codes (element 2i in the low byte) convert exactly to an
+// f16 pair in one instruction, and the dot products and the PV sums take f16 operands
+// with fp32 accumulation (mixed-precision fma), so no code is widened to fp32 on its own.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t pair) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(pair & 0xffffu)));
+  return r;
+}
+
+// VEC E4M3 codes from shared memory as VEC/2 f16 pairs.
+template <int VEC>
+__device__ __forceinline__ void load_row_h2(const uint8_t* p, uint32_t* h2) {
+  static_assert(VEC == 4 || VEC == 8 || VEC == 16, "E4M3 rows are read 4, 8 or 16 codes at a time");
+  if constexpr (VEC == 4) {
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(p);
+    h2[0] = e4m3x2_to_h2(x);
+    h2[1] = e4m3x2_to_h2(x >> 16);
+  } else if constexpr (VEC == 8) {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    h2[0] = e4m3x2_to_h2(x.x);
+    h2[1] = e4m3x2_to_h2(x.x >> 16);
+    h2[2] = e4m3x2_to_h2(x.y);
+    h2[3] = e4m3x2_to_h2(x.y >> 16);
+  } else {
+    const uint4 x = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h2[2 * i] = e4m3x2_to_h2(w[i]);
+      h2[2 * i + 1] = e4m3x2_to_h2(w[i] >> 16);
+    }
+  }
+}
+
+// lo += a.lo * b.lo, hi += a.hi * b.hi: f16 pairs in, fp32 sums.
+__device__ __forceinline__ void fma_h2_f32(uint32_t a, uint32_t b, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(a), "r"(b));
+}
+
+// The fp32 pair acc += (v.lo, v.hi) * p for an f16 pair v and an f16 scalar p.
+__device__ __forceinline__ uint64_t fma_h2s_f32x2(uint32_t v, unsigned short p, uint64_t acc) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc));
+  asm("{\n\t.reg .b16 vl, vh;\n\tmov.b32 {vl, vh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, vl, %3, %0;\n\tfma.rn.f32.f16 %1, vh, %3, %1;\n\t}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(v), "h"(p));
+  return pk2(lo, hi);
+}
+
+__device__ __forceinline__ unsigned short f16_bits(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
 template <typename T, int VEC>
 __device__ __forceinline__ void load_row_pairs(const T* p, uint64_t* f2) {
   if constexpr (sizeof(T) == 4) {
@@ -188,10 +252,12 @@ __device__ void write_group_const(const DecodeArgs& a, int b, int g, float o, fl
   }
 }
 
-template <typename T, int D, int P, int G, bool UNIFIED>
-__global__ void __launch_bounds__(DecodeCfg<T, D, P, G, UNIFIED>::THREADS, DecodeCfg<T, D, P, G, UNIFIED>::MIN_BLOCKS)
+template <typename T, int D, int P, int G, bool UNIFIED, bool FP8 = false>
+__global__ void __launch_bounds__(DecodeCfg<T, D, P, G, UNIFIED, FP8>::THREADS,
+                                  DecodeCfg<T, D, P, G, UNIFIED, FP8>::MIN_BLOCKS)
 decode_paged_kernel(const DecodeArgs a) {
-  using C = DecodeCfg<T, D, P, G, UNIFIED>;
+  using C = DecodeCfg<T, D, P, G, UNIFIED, FP8>;
+  using KV = typename C::KV;
   extern __shared__ __align__(128) unsigned char smem[];
   const int split = blockIdx.x;
   const int g = blockIdx.y;
@@ -265,6 +331,14 @@ decode_paged_kernel(const DecodeArgs a) {
           break;
         }
         if (elect_one()) {
+          if constexpr (FP8) {
+            // the stage's scales, published to the consumers by the arrive below
+            float* scl = reinterpret_cast<float*>(smem + C::SCALE_OFF) + 2 * s;
+            const bool bad_k = (badm >> k) & 1u;
+            const size_t si = (size_t)(bad_k ? 0 : p) * a.n_kv_heads + g;
+            scl[0] = bad_k ? 0.0f : __ldg(a.k_scale + si);
+            scl[1] = bad_k ? 0.0f : __ldg(a.v_scale + si);
+          }
           if ((badm >> k) & 1u) {
             mbar_arrive(bar_full + 8 * s);  // completes the phase with no data
           } else {
@@ -308,7 +382,10 @@ decode_paged_kernel(const DecodeArgs a) {
   float lsum_own = 0.0f;
 
   if (warp < C::NW) {
-    uint64_t q2[G][DP2];
+    // q as fp32 pairs prescaled by scale*log2(e); FP8: unscaled f16 pairs, the scale and
+    // the tile's k_scale multiply the finished dot product
+    using QP = std::conditional_t<FP8, uint32_t, uint64_t>;
+    QP q2[G][DP2];
     const float qscale = a.scale * kLog2e;
     const T* qp = static_cast<const T*>(a.q) + ((size_t)b * a.n_qo_heads + g * G) * D;
 #pragma unroll
@@ -318,7 +395,12 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int e = 0; e < C::VEC; e += 2) {
           const T* src = qp + gi * D + c * C::LPT * C::VEC + j * C::VEC + e;
-          q2[gi][(c * C::VEC + e) / 2] = pk2(to_f32<T>(src[0]) * qscale, to_f32<T>(src[1]) * qscale);
+          if constexpr (FP8) {
+            const __half2 h = __floats2half2_rn(to_f32<T>(src[0]), to_f32<T>(src[1]));
+            q2[gi][(c * C::VEC + e) / 2] = *reinterpret_cast<const uint32_t*>(&h);
+          } else {
+            q2[gi][(c * C::VEC + e) / 2] = pk2(to_f32<T>(src[0]) * qscale, to_f32<T>(src[1]) * qscale);
+          }
         }
 
     const float beta2 = kUnifiedBeta * kLog2e;
@@ -332,8 +414,15 @@ decode_paged_kernel(const DecodeArgs a) {
         }
         break;
       }
-      const T* kt = reinterpret_cast<const T*>(smem + s * C::TILE);
-      const T* vt = reinterpret_cast<const T*>(smem + (C::NSTAGE + s) * C::TILE);
+      const KV* kt = reinterpret_cast<const KV*>(smem + s * C::TILE);
+      const KV* vt = reinterpret_cast<const KV*>(smem + (C::NSTAGE + s) * C::TILE);
+      // FP8: this stage's tile scales (1 otherwise; multiplied in only for FP8)
+      float ks = 1.0f, vs = 1.0f;
+      if constexpr (FP8) {
+        const float* scl = reinterpret_cast<const float*>(smem + C::SCALE_OFF) + 2 * s;
+        ks = scl[0];
+        vs = scl[1];
+      }
       const int valid = min(P, kv_len - (first + i) * P);
 #pragma unroll
       for (int ch = 0; ch < C::NCHUNK; ++ch) {
@@ -341,17 +430,28 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
         for (int it = 0; it < C::NIT; ++it) {
           const int t = (ch * C::NIT + it) * C::TPI + tg;
-          uint64_t k2[DP2];
+          QP k2[DP2];
 #pragma unroll
-          for (int c = 0; c < C::NV; ++c)
-            load_row_pairs<T, C::VEC>(kt + t * D + c * C::LPT * C::VEC + j * C::VEC, k2 + c * C::VEC / 2);
+          for (int c = 0; c < C::NV; ++c) {
+            if constexpr (FP8)
+              load_row_h2<C::VEC>(kt + t * D + c * C::LPT * C::VEC + j * C::VEC, k2 + c * C::VEC / 2);
+            else
+              load_row_pairs<KV, C::VEC>(kt + t * D + c * C::LPT * C::VEC + j * C::VEC, k2 + c * C::VEC / 2);
+          }
 #pragma unroll
           for (int gi = 0; gi < G; ++gi) {
-            uint64_t d2 = 0ull;
+            if constexpr (FP8) {
+              float d0 = 0.0f, d1 = 0.0f;
 #pragma unroll
-            for (int e = 0; e < DP2; ++e) d2 = ffma2(q2[gi][e], k2[e], d2);
-            const float2 d = upk2(d2);
-            sc[it][gi] = d.x + d.y;
+              for (int e = 0; e < DP2; ++e) fma_h2_f32(q2[gi][e], k2[e], d0, d1);
+              sc[it][gi] = (d0 + d1) * (qscale * ks);
+            } else {
+              uint64_t d2 = 0ull;
+#pragma unroll
+              for (int e = 0; e < DP2; ++e) d2 = ffma2(q2[gi][e], k2[e], d2);
+              const float2 d = upk2(d2);
+              sc[it][gi] = d.x + d.y;
+            }
           }
         }
         if constexpr (C::SCATTER) {
@@ -438,16 +538,26 @@ decode_paged_kernel(const DecodeArgs a) {
             float pw[G];
 #pragma unroll
             for (int gi = 0; gi < G; ++gi) pw[gi] = __shfl_sync(0xffffffffu, so[it], tg * C::LPT + gi * LPH);
-            uint64_t v2[DP2];
+            QP v2[DP2];
 #pragma unroll
-            for (int c = 0; c < C::NV; ++c)
-              load_row_pairs<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+            for (int c = 0; c < C::NV; ++c) {
+              if constexpr (FP8)
+                load_row_h2<C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+              else
+                load_row_pairs<KV, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+            }
             if (t < valid) {
 #pragma unroll
               for (int gi = 0; gi < G; ++gi) {
-                const uint64_t p2 = pk2(pw[gi], pw[gi]);
+                if constexpr (FP8) {
+                  const unsigned short ph = f16_bits(pw[gi] * vs);
 #pragma unroll
-                for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+                  for (int e = 0; e < DP2; ++e) acc2[gi][e] = fma_h2s_f32x2(v2[e], ph, acc2[gi][e]);
+                } else {
+                  const uint64_t p2 = pk2(pw[gi], pw[gi]);
+#pragma unroll
+                  for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+                }
               }
             }
           }
@@ -536,16 +646,26 @@ decode_paged_kernel(const DecodeArgs a) {
 #pragma unroll
           for (int it = 0; it < C::NIT; ++it) {
             const int t = (ch * C::NIT + it) * C::TPI + tg;
-            uint64_t v2[DP2];
+            QP v2[DP2];
 #pragma unroll
-            for (int c = 0; c < C::NV; ++c)
-              load_row_pairs<T, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+            for (int c = 0; c < C::NV; ++c) {
+              if constexpr (FP8)
+                load_row_h2<C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+              else
+                load_row_pairs<KV, C::VEC>(vt + t * D + c * C::LPT * C::VEC + j * C::VEC, v2 + c * C::VEC / 2);
+            }
             if (t < valid) {
 #pragma unroll
               for (int gi = 0; gi < G; ++gi) {
-                const uint64_t p2 = pk2(sc[it][gi], sc[it][gi]);
+                if constexpr (FP8) {
+                  const unsigned short ph = f16_bits(sc[it][gi] * vs);
 #pragma unroll
-                for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+                  for (int e = 0; e < DP2; ++e) acc2[gi][e] = fma_h2s_f32x2(v2[e], ph, acc2[gi][e]);
+                } else {
+                  const uint64_t p2 = pk2(sc[it][gi], sc[it][gi]);
+#pragma unroll
+                  for (int e = 0; e < DP2; ++e) acc2[gi][e] = ffma2(p2, v2[e], acc2[gi][e]);
+                }
               }
             }
           }
@@ -669,10 +789,10 @@ decode_paged_kernel(const DecodeArgs a) {
   }
 }
 
-template <typename T, int D, int P, int G, bool UNIFIED>
+template <typename T, int D, int P, int G, bool UNIFIED, bool FP8 = false>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
-  using C = DecodeCfg<T, D, P, G, UNIFIED>;
-  auto kern = decode_paged_kernel<T, D, P, G, UNIFIED>;
+  using C = DecodeCfg<T, D, P, G, UNIFIED, FP8>;
+  auto kern = decode_paged_kernel<T, D, P, G, UNIFIED, FP8>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
   cudaGetDevice(&dev);
@@ -686,9 +806,9 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   return check_launch(cudaGetLastError());
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool FP8 = false>
 constexpr int ctas_per_sm_t() {
-  using C = DecodeCfg<T, D, 16, G>;
+  using C = DecodeCfg<T, D, 16, G, false, FP8>;
   constexpr int by_smem = (227 * 1024) / C::SMEM;
   return by_smem < C::MIN_BLOCKS ? by_smem : C::MIN_BLOCKS;
 }

@@ -32,6 +32,10 @@ struct DecodeArgs {
   bool unified;
   float phi;
   int32_t* fallback_count;
+  // FP8 E4M3 page pools (q and out are bf16): one scale per (page, KV head) of K and V
+  bool fp8;
+  const float* k_scale;  // [num_pages][n_kv_heads]
+  const float* v_scale;
 };
 
 struct SplitPlan {

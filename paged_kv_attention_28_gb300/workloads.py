@@ -23,6 +23,13 @@ kernel that reads them shows it in its output. Unused block-table entries are
 
 bf16 cases draw fp32 normals and round them to bf16 (round to nearest even);
 the oracle then receives the rounded values widened to fp64.
+
+FP8 cases hold E4M3 codes (bytes) in their page pools and one float32 scale per
+(page, KV head) tile of K and of V, ``[num_pages, Hkv]``. A tile's scale is its
+largest magnitude over 448, the largest finite E4M3 value, and its codes are the
+fp32 normals divided by the scale and rounded to E4M3 (torch's conversion). That
+is input preparation; the oracle and the kernel both read the codes and scales.
+Poisoned slots hold the NaN code 0x7F.
 """
 from __future__ import annotations
 
@@ -96,6 +103,53 @@ class PagedDecodeCase:
         """K and V bytes that attention must read once: sum of lengths x Hkv x D x 2 tensors."""
         esize = self.k_pages.element_size()
         return int(self.kv_lens.to(torch.int64).sum()) * self.n_kv_heads * self.head_dim * esize * 2
+
+
+@dataclass
+class PagedDecodeFp8Case:
+    q: torch.Tensor            # bf16 [B, Hq, D]
+    k_codes: torch.Tensor      # uint8 [num_pages, Hkv, P, D] (E4M3)
+    v_codes: torch.Tensor
+    k_scale: torch.Tensor      # float32 [num_pages, Hkv]
+    v_scale: torch.Tensor
+    block_table: torch.Tensor  # int32 [B, max_blocks]
+    kv_lens: torch.Tensor      # int32 [B]
+    scale: float
+    name: str = ""
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def n_qo_heads(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def head_dim(self) -> int:
+        return self.q.shape[2]
+
+    @property
+    def num_pages(self) -> int:
+        return self.k_codes.shape[0]
+
+    @property
+    def n_kv_heads(self) -> int:
+        return self.k_codes.shape[1]
+
+    @property
+    def page_size(self) -> int:
+        return self.k_codes.shape[2]
+
+    @property
+    def max_blocks(self) -> int:
+        return self.block_table.shape[1]
+
+    def kv_bytes(self) -> int:
+        """Codes of every token's K and V plus the K and V scales of every page read."""
+        toks = int(self.kv_lens.sum())
+        pages = int(((self.kv_lens + self.page_size - 1) // self.page_size).sum())
+        return toks * self.n_kv_heads * self.head_dim * 2 + pages * self.n_kv_heads * 4 * 2
 
 
 @dataclass
@@ -260,6 +314,69 @@ def make_paged_decode(seed: int, batch: int, n_qo_heads: int, n_kv_heads: int, h
                            float(scale), name=name)
 
 
+def make_paged_decode_fp8(seed: int, batch: int, n_qo_heads: int, n_kv_heads: int, head_dim: int,
+                          page_size: int, kv_lens, num_pages: int | None = None,
+                          max_blocks: int | None = None, q_std: float = 1.0, k_std: float = 1.0,
+                          v_std: float = 1.0, scale: float | None = None, poison: bool = True,
+                          name: str = "") -> PagedDecodeFp8Case:
+    """Build a paged decode batch over FP8 E4M3 pages with per-(page, KV head) scales.
+
+    The lengths, page order and query follow ``make_paged_decode`` for the same seed
+    (q rounded to bf16); the pages hold E4M3 codes of fp32 normals.
+    """
+    g = _gen(seed)
+    if isinstance(kv_lens, tuple):
+        lo, hi = kv_lens
+        lens = torch.randint(lo, hi + 1, (batch,), generator=g, dtype=torch.int64).tolist()
+    else:
+        lens = [int(x) for x in kv_lens]
+    assert len(lens) == batch
+    nblk = [(l + page_size - 1) // page_size for l in lens]
+    if max_blocks is None:
+        max_blocks = max(1, max(nblk))
+    assert max(nblk) <= max_blocks
+    need = sum(nblk)
+    if num_pages is None:
+        num_pages = max(1, need)
+    assert need <= num_pages, "pool too small"
+    q = _normal(g, (batch, n_qo_heads, head_dim), q_std, torch.bfloat16)
+    order = torch.randperm(num_pages, generator=g)[:need].tolist()
+    pages, pos = [], 0
+    for n in nblk:
+        pages.append(order[pos:pos + n])
+        pos += n
+    shape = (num_pages, n_kv_heads, page_size, head_dim)
+    fill = 0x7F if poison else 0
+    k_codes = torch.full(shape, fill, dtype=torch.uint8)
+    v_codes = torch.full(shape, fill, dtype=torch.uint8)
+    k_scale = torch.ones((num_pages, n_kv_heads), dtype=torch.float32)
+    v_scale = torch.ones((num_pages, n_kv_heads), dtype=torch.float32)
+    flat = [p for seq in pages for p in seq]
+    for start in range(0, len(flat), 1024):
+        idx = torch.tensor(flat[start:start + 1024], dtype=torch.int64)
+        for codes, sc, std in ((k_codes, k_scale, k_std), (v_codes, v_scale, v_std)):
+            x = _normal(g, (len(idx), n_kv_heads, page_size, head_dim), std, torch.float32)
+            amax = x.abs().amax(dim=(2, 3))
+            s = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+            y = (x / s[:, :, None, None]).clamp(-448.0, 448.0)
+            codes[idx] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+            sc[idx] = s
+    if poison:
+        for seq, length in zip(pages, lens):
+            tail = length % page_size
+            if seq and tail:
+                k_codes[seq[-1], :, tail:, :] = 0x7F
+                v_codes[seq[-1], :, tail:, :] = 0x7F
+    table = torch.full((batch, max_blocks), -1, dtype=torch.int32)
+    for b, seq in enumerate(pages):
+        if seq:
+            table[b, :len(seq)] = torch.tensor(seq, dtype=torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    return PagedDecodeFp8Case(q, k_codes, v_codes, k_scale, v_scale, table,
+                              torch.tensor(lens, dtype=torch.int32), float(scale), name=name)
+
+
 def make_prefill(seed: int, batch: int, seq_len: int, n_qo_heads: int, n_kv_heads: int,
                  head_dim: int, dtype: str = "bf16", std: float = 1.0,
                  scale: float | None = None, name: str = "") -> PrefillCase:
@@ -334,6 +451,12 @@ def llama7b_batched_decode(poison: bool = True) -> PagedDecodeCase:
     return make_paged_decode(1002, 16, 32, 32, 128, 16, (512, 4096), num_pages=8192,
                              max_blocks=256, dtype="bf16", poison=poison,
                              name="llama7b_batched_decode")
+
+
+def llama7b_batched_decode_fp8(poison: bool = True) -> PagedDecodeFp8Case:
+    """The Llama-7B batch's shape over FP8 E4M3 pages (same lengths and page order)."""
+    return make_paged_decode_fp8(1002, 16, 32, 32, 128, 16, (512, 4096), num_pages=8192,
+                                 max_blocks=256, poison=poison, name="llama7b_batched_decode_fp8")
 
 
 def long_context_gqa_decode(poison: bool = True) -> PagedDecodeCase:

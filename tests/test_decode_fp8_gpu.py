@@ -1,0 +1,107 @@
+"""GPU parity of attn_decode_paged_fp8 (E4M3 page pools with per-(page, KV head) scales)
+against the fp64 oracle's decode over the dequantised pages, on the same seeded codes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_28_gb300 import workloads
+from tests._compare import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def b():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_attention_28_gb300 import build
+    build.build(quiet=True)
+    from paged_kv_attention_28_gb300 import binding
+    return binding
+
+
+def to_dev(c):
+    return tuple(t.to("cuda") for t in (c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                        c.block_table, c.kv_lens))
+
+
+def run(b, c, splits=0, dev=None, table=None):
+    q, kc, vc, ks, vs, bt, ln = dev if dev is not None else to_dev(c)
+    if table is not None:
+        bt = table.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = b.decode_paged_fp8(q, kc, vc, ks, vs, bt, ln, c.scale, num_splits=splits, err_flag=err)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy(), int(err.item())
+
+
+def ref(c, rows=None, table=None):
+    return oracle.decode_paged_fp8(c.q.double().numpy(), c.k_codes.numpy(), c.v_codes.numpy(),
+                                   c.k_scale.numpy(), c.v_scale.numpy(),
+                                   (c.block_table if table is None else table).numpy(),
+                                   c.kv_lens.numpy(), c.scale, rows=rows)
+
+
+def check(got, want, what):
+    assert_close(got[0], want[0], "bf16", what + " out")
+    assert_close(got[1], want[1], "bf16", what + " lse")
+
+
+def test_llama7b_batched_decode_fp8_all_rows(b):
+    c = workloads.llama7b_batched_decode_fp8()
+    dev = to_dev(c)
+    want = ref(c)
+    for splits in (0, 1, 8):
+        got = run(b, c, splits, dev=dev)
+        assert got[2] == 0
+        check(got, want, f"llama7b_batched_decode_fp8 splits={splits}")
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_decode_fp8_shapes(b, head_dim, group):
+    hkv = 2
+    lens = [1, 15, 16, 17, 100, 257, 0, 48]
+    c = workloads.make_paged_decode_fp8(70 + group + head_dim, len(lens), hkv * group, hkv, head_dim,
+                                        16, lens, num_pages=64, max_blocks=20)
+    want = ref(c)
+    for splits in (0, 1, 3):
+        got = run(b, c, splits)
+        assert got[2] == 0
+        check(got, want, f"fp8 D={head_dim} G={group} splits={splits}")
+
+
+def test_decode_fp8_wide_scales_and_logits(b):
+    # k ~ 3 N(0,1) spreads the logits; the per-tile scales then span a wide range too
+    c = workloads.make_paged_decode_fp8(71, 4, 32, 8, 128, 16, [3000, 1, 700, 2049], num_pages=512,
+                                        k_std=3.0, v_std=0.5)
+    want = ref(c)
+    for splits in (0, 16):
+        got = run(b, c, splits)
+        assert got[2] == 0
+        check(got, want, f"fp8 wide splits={splits}")
+
+
+def test_decode_fp8_bad_page_sets_flag(b):
+    c = workloads.make_paged_decode_fp8(72, 3, 4, 2, 64, 16, [40, 40, 40], num_pages=12, max_blocks=4)
+    table = c.block_table.clone()
+    table[1, 1] = c.num_pages + 5               # out of range, inside the sequence
+    table[2, 3] = 10**6                         # out of range but past the length: never read
+    for splits in (1, 2):
+        out, lse, err = run(b, c, splits, table=table)
+        assert err & b.PKV_DEVERR_BAD_PAGE
+        assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
+        want = ref(c, rows=[(bb, h) for bb in (0, 2) for h in range(4)], table=table)
+        check((out[[0, 2]], lse[[0, 2]]), (want[0][[0, 2]], want[1][[0, 2]]), "fp8 good rows")
+
+
+def test_decode_fp8_rejects_missing_scales(b):
+    c = workloads.make_paged_decode_fp8(73, 1, 4, 4, 64, 16, [20], num_pages=4)
+    q, kc, vc, ks, vs, bt, ln = to_dev(c)
+    L = b.lib
+    p = lambda t: None if t is None else __import__("ctypes").c_void_p(t.data_ptr())
+    st = L.attn_decode_paged_fp8(p(q), p(kc), p(vc), None, p(vs), p(bt), p(ln), p(q), None, 1,
+                                 bt.shape[1], c.num_pages, 4, 4, 64, 16, c.scale, 1, None, 0, None,
+                                 None)
+    assert st == b.PKV_ERR_INVALID_ARG

@@ -652,3 +652,147 @@ def test_named_workload_shapes():
     assert int(c1.kv_lens[0]) == 256 and c1.max_blocks == 16
     used = c1.block_table[0].tolist()
     assert len(set(used)) == 16 and all(0 <= p < 64 for p in used)
+
+
+# ----------------------------------------------------------------------------- FP8 E4M3 pages
+
+def check_e4m3_worked_values(f):
+    # values fixed by the format: bias 7, 3 mantissa bits, subnormals at exponent 0,
+    # NaN at exponent 15 / mantissa 7, no infinities
+    want = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x30: 0.5, 0x7E: 448.0, 0x08: 2.0 ** -6,
+            0x07: 7 * 2.0 ** -9, 0x01: 2.0 ** -9, 0xB8: -1.0, 0xFE: -448.0, 0x78: 256.0}
+    v = f(np.array(list(want)))
+    ok = np.array_equal(v, np.array(list(want.values())))
+    neg_zero = f(np.array([0x80]))[0]
+    return bool(ok and neg_zero == 0.0 and np.signbit(neg_zero) and np.isnan(f(np.array([0x7F, 0xFF]))).all())
+
+
+def check_e4m3_matches_library(f):
+    # every code against torch's float8_e4m3fn conversion (a library routine)
+    torch = pytest.importorskip("torch")
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().double().numpy()
+    v = f(np.arange(256))
+    return bool(((v == lib) | (np.isnan(v) & np.isnan(lib))).all())
+
+
+def check_e4m3_monotone_and_symmetric(f):
+    pos = f(np.arange(0x7F))          # 0x00 .. 0x7E: every finite non-negative value
+    neg = f(np.arange(0x80, 0xFF))
+    return bool(np.all(np.diff(pos) > 0) and np.array_equal(neg, -pos))
+
+
+FP8_VALUE_PINS = [check_e4m3_worked_values, check_e4m3_matches_library, check_e4m3_monotone_and_symmetric]
+
+
+def _fp8_case(seed, B=3, Hq=8, Hkv=2, D=16, P=4, lens=(9, 1, 14), n_pages=12):
+    r = np.random.default_rng(seed)
+    codes_k = r.integers(0, 256, size=(n_pages, Hkv, P, D))
+    codes_v = r.integers(0, 256, size=(n_pages, Hkv, P, D))
+    # no NaN codes (exponent 15, mantissa 7) in real pages
+    codes_k[(codes_k & 0x7F) == 0x7F] = 0x3F
+    codes_v[(codes_v & 0x7F) == 0x7F] = 0x3F
+    ks = r.uniform(1e-3, 2e-2, size=(n_pages, Hkv))
+    vs = r.uniform(1e-3, 2e-2, size=(n_pages, Hkv))
+    table = np.stack([r.permutation(n_pages)[:4] for _ in range(B)])
+    q = r.normal(size=(B, Hq, D))
+    return q, codes_k, codes_v, ks, vs, table, np.array(lens), 0.3
+
+
+def check_fp8_decode_is_decode_of_dequantised_pages(f):
+    # the dequantised pools are built here from torch's float8 conversion and the scales,
+    # independently of the oracle's e4m3 function, then fed to the plain decode
+    torch = pytest.importorskip("torch")
+    q, ck, cv, ks, vs, table, lens, scale = _fp8_case(7)
+    to_f = lambda c: torch.from_numpy(c.astype(np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    kf = to_f(ck) * ks[:, :, None, None]
+    vf = to_f(cv) * vs[:, :, None, None]
+    want = oracle.decode_paged(q, kf, vf, table, lens, scale)
+    got = f(q, ck, cv, ks, vs, table, lens, scale)
+    return np.allclose(got[0], want[0], atol=1e-12) and np.allclose(got[1], want[1], atol=1e-12)
+
+
+def check_fp8_scale_invariances(f):
+    # a common factor on every V scale scales the output; one on every K scale is the same
+    # as a larger softmax scale
+    q, ck, cv, ks, vs, table, lens, scale = _fp8_case(8)
+    base = f(q, ck, cv, ks, vs, table, lens, scale)
+    v3 = f(q, ck, cv, ks, vs * 3.0, table, lens, scale)
+    k2 = f(q, ck, cv, ks * 2.0, vs, table, lens, scale)
+    s2 = f(q, ck, cv, ks, vs, table, lens, scale * 2.0)
+    return (np.allclose(v3[0], 3.0 * base[0], atol=1e-12) and np.allclose(v3[1], base[1], atol=1e-12)
+            and np.allclose(k2[0], s2[0], atol=1e-12) and np.allclose(k2[1], s2[1], atol=1e-12))
+
+
+def check_fp8_per_tile_scale(f):
+    # doubling the scale of one (page, KV head) tile of V changes exactly the rows that read it
+    q, ck, cv, ks, vs, table, lens, scale = _fp8_case(9)
+    base = f(q, ck, cv, ks, vs, table, lens, scale)
+    page = int(table[0, 0])
+    vs2 = vs.copy()
+    vs2[page, 1] *= 2.0
+    got = f(q, ck, cv, ks, vs2, table, lens, scale)
+    G = q.shape[1] // ck.shape[1]
+    readers = {(b, h) for b in range(q.shape[0]) for h in range(q.shape[1])
+               if h // G == 1 and page in set(table[b, : (lens[b] + 3) // 4].tolist())}
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            same = np.allclose(got[0][b, h], base[0][b, h], atol=1e-14)
+            if same == ((b, h) in readers):
+                return False
+    return bool(readers)
+
+
+FP8_DECODE_PINS = [check_fp8_decode_is_decode_of_dequantised_pages, check_fp8_scale_invariances,
+                   check_fp8_per_tile_scale]
+
+
+@pytest.mark.parametrize("pin", FP8_VALUE_PINS)
+def test_e4m3_pins(pin):
+    assert pin(oracle.e4m3_to_float)
+
+
+@pytest.mark.parametrize("pin", FP8_DECODE_PINS)
+def test_fp8_decode_pins(pin):
+    assert pin(oracle.decode_paged_fp8)
+
+
+def _e4m3_mutant(kind):
+    def f(codes):
+        c = np.asarray(codes).astype(np.int64) & 0xFF
+        s, e, m = (c >> 7) & 1, (c >> 3) & 0xF, (c & 7).astype(np.float64)
+        bias = 8 if kind == "bias" else 7
+        if kind == "no_subnormal":
+            mag = np.ldexp(1.0 + m / 8.0, e - bias)
+        else:
+            mag = np.where(e == 0, np.ldexp(m / 8.0, 1 - bias), np.ldexp(1.0 + m / 8.0, e - bias))
+        if kind == "mantissa4":
+            mag = np.where(e == 0, np.ldexp(m / 16.0, 1 - bias), np.ldexp(1.0 + m / 16.0, e - bias))
+        val = mag if kind == "no_sign" else np.where(s == 1, -mag, mag)
+        if kind != "no_nan":
+            val = np.where((e == 15) & (c & 7 == 7), np.nan, val)
+        return val
+    return f
+
+
+def _fp8_decode_mutant(kind):
+    def f(q, ck, cv, ks, vs, table, lens, scale):
+        if kind == "scale_transposed":
+            ks2 = ks.copy()
+            ks2[: ks.shape[1], :] = ks[: ks.shape[1], :][:, ::-1]
+            ks = ks2
+        if kind == "k_scale_for_v":
+            vs = ks
+        if kind == "page_not_logical":   # scale read by logical block index instead of page
+            ks = np.roll(ks, 1, axis=0)
+        return oracle.decode_paged_fp8(q, ck, cv, ks, vs, table, lens, scale)
+    return f
+
+
+@pytest.mark.parametrize("kind", ["bias", "no_subnormal", "mantissa4", "no_sign", "no_nan"])
+def test_e4m3_planted_mistakes_are_caught(kind):
+    assert not all(pin(_e4m3_mutant(kind)) for pin in FP8_VALUE_PINS)
+
+
+@pytest.mark.parametrize("kind", ["scale_transposed", "k_scale_for_v", "page_not_logical"])
+def test_fp8_decode_planted_mistakes_are_caught(kind):
+    assert not all(pin(_fp8_decode_mutant(kind)) for pin in FP8_DECODE_PINS)
