@@ -208,8 +208,9 @@ int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void
  *     attn_decode_workspace_size(..., PKV_FP8_E4M3).
  * The result is the attention of attn_decode_paged over the dequantised values, with
  * the per-tile scales applied to the dot products and to the softmax weights. Pools
- * must be 16-byte aligned. Built for head_dim 64 and 128, page_size 16 and GQA
- * groups 1, 2, 4 and 8; other shapes return PKV_ERR_UNSUPPORTED.
+ * must be 16-byte aligned. A CTA takes two adjacent KV heads, so n_kv_heads must be
+ * even. Built for head_dim 64 and 128, page_size 16 and GQA groups 1, 2, 4 and 8;
+ * other shapes return PKV_ERR_UNSUPPORTED.
  */
 int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
                           const float* k_scale, const float* v_scale, const int32_t* block_table,

@@ -100,7 +100,9 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   const int G = c.n_qo_heads / c.n_kv_heads;
   if (!decode_supported(c.dtype, c.head_dim, c.page_size, G)) return PKV_ERR_UNSUPPORTED;
   if (c.batch > 65535 || c.n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-  const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, c.n_kv_heads, c.num_splits,
+  if (fp8 && c.n_kv_heads % 2) return PKV_ERR_UNSUPPORTED;  // two KV heads per CTA
+  const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, fp8 ? c.n_kv_heads / 2 : c.n_kv_heads,
+                                            c.num_splits,
                                             decode_ctas_per_sm(fp8 ? PKV_FP8_E4M3 : c.dtype, c.head_dim, G));
   const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.head_dim, plan.num_splits);
   if (need > 0 && (!c.workspace || c.workspace_bytes < need ||
@@ -172,7 +174,10 @@ int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, in
       head_dim < 1 || page_size < 1 || num_splits < 0 || n_qo_heads % n_kv_heads)
     return PKV_ERR_INVALID_ARG;
   if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
-  return plan_decode_splits(batch, max_blocks_per_seq, n_kv_heads, num_splits,
+  if (dtype == PKV_FP8_E4M3 && n_kv_heads % 2) return PKV_ERR_UNSUPPORTED;
+  // the FP8 kernel's CTA takes two KV heads
+  return plan_decode_splits(batch, max_blocks_per_seq, dtype == PKV_FP8_E4M3 ? n_kv_heads / 2 : n_kv_heads,
+                            num_splits,
                             decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads))
       .num_splits;
 }

@@ -8,7 +8,8 @@ namespace pkv {
 
 int dispatch_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {
   const int G = a.n_qo_heads / a.n_kv_heads;
-  if (a.page_size != 16 || a.dtype != PKV_BF16 || a.unified) return PKV_ERR_UNSUPPORTED;
+  // a CTA takes two adjacent KV heads (one copy moves both heads' tiles of a page)
+  if (a.page_size != 16 || a.dtype != PKV_BF16 || a.unified || a.n_kv_heads % 2) return PKV_ERR_UNSUPPORTED;
 #define PKV_FP8_CASE(DD, GG) \
   if (a.head_dim == DD && G == GG) return launch_decode_t<__nv_bfloat16, DD, 16, GG, false, true>(a, stream);
   PKV_FP8_CASE(64, 1) PKV_FP8_CASE(64, 2) PKV_FP8_CASE(64, 4) PKV_FP8_CASE(64, 8)

@@ -48,9 +48,10 @@ constexpr float kUnifiedBeta = 60.0f;
 // measured 5 % slower on the unified-max variant and 5 % slower on the online one).
 // FP8: the page pools hold E4M3 codes with one float scale per (page, KV head) tile of K
 // and of V; q and the output stay T (bf16). A stage then carries half the bytes and the
-// CTA half the shared memory, and the work per page is what limits a CTA (the same
-// tokens as bf16 took as long with a ring twice as deep), so G = 1 runs six CTAs per SM
-// (measured: 3 -> 130 us, 5 -> 102 us, 6 -> 93 us, 7 -> 106 us on the Llama-7B batch).
+// CTA half the shared memory. A CTA takes two adjacent KV heads so that each bulk copy
+// still moves 4 KiB (both heads' tiles of a page); with 2 KiB copies the batch ran at half
+// the DRAM throughput. G = 1 runs six CTAs per SM. Measured on the Llama-7B batch: one head
+// per CTA with 3, 5, 6, 7 CTAs per SM 130, 102, 93, 106 us; two heads per CTA 77 us.
 template <typename T, int D, int P, int G, bool UNIFIED = false, bool FP8 = false>
 struct DecodeCfg {
   using KV = std::conditional_t<FP8, uint8_t, T>;  // element type of the page pools
@@ -65,25 +66,31 @@ struct DecodeCfg {
   static constexpr int NIT = ITERS < NIT_MAX ? ITERS : NIT_MAX;  // steps per softmax chunk
   static constexpr int NCHUNK = ITERS / NIT;
   static constexpr int TILE = P * D * ES;          // bytes of one (page, KV head) tile
+  // FP8: a CTA takes two adjacent KV heads, so one bulk copy moves both heads' tiles of a
+  // page (2 x 2 KiB, contiguous in the pool) instead of two copies of 2 KiB.
+  static constexpr int HPC = FP8 ? 2 : 1;          // KV heads per CTA
+  static constexpr int STAGE = HPC * TILE;         // bytes of K (or V) in one ring stage
   static constexpr int NW = 4;                     // consumer warps
+  static constexpr int WPH = NW / HPC;             // consumer warps per KV head
   // bf16 with one query head per KV head: a 4-stage ring and five CTAs per SM keep more
   // pages in flight per SM than 8 stages and three CTAs (measured 6359 against 6259 GB/s
   // on the Llama-7B batch; 4 stages and four CTAs 6012).
-  static constexpr int NSTAGE = (G == 1 && !FP8 && sizeof(T) == 2) ? 4 : 8;  // multiple of NW
+  static constexpr int NSTAGE = (G == 1 && sizeof(T) == 2) ? 4 : 8;  // multiple of NW
   static constexpr int THREADS = (NW + 1) * 32;
   static constexpr int MIN_BLOCKS = G >= 8 ? 2 : G > 1 ? 3 : FP8 ? 6 : sizeof(T) == 2 ? 5 : 3;
   // G >= 4: the row's lanes reduce the G dot products by halving exchanges, after which
   // each lane holds one head's full score (reduce_scatter_heads).
   static constexpr bool SCATTER = G >= 4 && G <= LPT;
-  static constexpr int BAR_OFF = 2 * NSTAGE * TILE;
+  static constexpr int BAR_OFF = 2 * NSTAGE * STAGE;
   static constexpr int FLAG_OFF = BAR_OFF + 2 * NSTAGE * 8;
   static constexpr int SCALE_OFF = FLAG_OFF + 16;  // FP8: (k_scale, v_scale) of each stage
-  static constexpr int SMEM = SCALE_OFF + (FP8 ? NSTAGE * 8 : 0);
+  static constexpr int SMEM = SCALE_OFF + (FP8 ? NSTAGE * HPC * 8 : 0);
   static_assert(D % LPT == 0 && DPL % VEC == 0 && VEC % 2 == 0, "head_dim split");
   static_assert(P % TPI == 0 && ITERS % NIT == 0, "page split");
   static_assert(NSTAGE % NW == 0, "stage ownership");
   static_assert(TILE % 16 == 0, "bulk copy granularity");
-  static_assert(NW * G * (D + 2) * 4 <= 2 * NSTAGE * TILE, "combine scratch fits in the ring");
+  static_assert(NW * G * (D + 2) * 4 <= 2 * NSTAGE * STAGE, "combine scratch fits in the ring");
+  static_assert(NW % HPC == 0 && NSTAGE % WPH == 0, "stage ownership per head");
 };
 
 __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
@@ -264,23 +271,27 @@ decode_paged_kernel(const DecodeArgs a) {
   using KV = typename C::KV;
   extern __shared__ __align__(128) unsigned char smem[];
   const int split = blockIdx.x;
-  const int g = blockIdx.y;
+  const int g0 = blockIdx.y * C::HPC;  // first KV head of this CTA
   const int b = blockIdx.z;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int hh = warp < C::NW ? warp / C::WPH : 0;  // a consumer warp's head within the CTA
+  const int g = g0 + hh;
 
   const int kv_len = __ldg(a.kv_lens + b);
   if (kv_len < 0 || kv_len > a.max_blocks * P) {
     if (split == 0) {
       if (threadIdx.x == 0) set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
-      if (!a.partial_only) write_group_const<T, D, G>(a, b, g, NAN, NAN);
+      if (!a.partial_only)
+        for (int k = 0; k < C::HPC; ++k) write_group_const<T, D, G>(a, b, g0 + k, NAN, NAN);
     }
     return;
   }
   const int nblk = (kv_len + P - 1) / P;
   const int n_live = (nblk + a.pages_per_split - 1) / a.pages_per_split;
   if (n_live == 0) {
-    if (split == 0 && !a.partial_only) write_group_const<T, D, G>(a, b, g, 0.0f, -INFINITY);
+    if (split == 0 && !a.partial_only)
+      for (int k = 0; k < C::HPC; ++k) write_group_const<T, D, G>(a, b, g0 + k, 0.0f, -INFINITY);
     return;
   }
   if (split >= n_live) return;
@@ -295,7 +306,7 @@ decode_paged_kernel(const DecodeArgs a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, C::HPC);  // one arrival from each head's consumer
     }
     flags->abort_ = 0;
     flags->bad_page = 0;
@@ -336,20 +347,23 @@ decode_paged_kernel(const DecodeArgs a) {
         }
         if (elect_one()) {
           if constexpr (FP8) {
-            // the stage's scales, published to the consumers by the arrive below
-            float* scl = reinterpret_cast<float*>(smem + C::SCALE_OFF) + 2 * s;
+            // the stage's scales (per head of the CTA), published by the arrive below
+            float* scl = reinterpret_cast<float*>(smem + C::SCALE_OFF) + 2 * C::HPC * s;
             const bool bad_k = (badm >> k) & 1u;
-            const size_t si = (size_t)(bad_k ? 0 : p) * a.n_kv_heads + g;
-            scl[0] = bad_k ? 0.0f : __ldg(a.k_scale + si);
-            scl[1] = bad_k ? 0.0f : __ldg(a.v_scale + si);
+            for (int h2 = 0; h2 < C::HPC; ++h2) {
+              const size_t si = (size_t)(bad_k ? 0 : p) * a.n_kv_heads + g0 + h2;
+              scl[2 * h2] = bad_k ? 0.0f : __ldg(a.k_scale + si);
+              scl[2 * h2 + 1] = bad_k ? 0.0f : __ldg(a.v_scale + si);
+            }
           }
           if ((badm >> k) & 1u) {
             mbar_arrive(bar_full + 8 * s);  // completes the phase with no data
           } else {
-            const size_t off = ((size_t)p * a.n_kv_heads + g) * C::TILE;
-            mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::TILE);
-            bulk_g2s_hint(sbase + s * C::TILE, kbase + off, C::TILE, bar_full + 8 * s, pol);
-            bulk_g2s_hint(sbase + (C::NSTAGE + s) * C::TILE, vbase + off, C::TILE,
+            // the CTA's HPC heads' tiles of a page are adjacent in the pool: one copy each
+            const size_t off = ((size_t)p * a.n_kv_heads + g0) * C::TILE;
+            mbar_arrive_expect_tx(bar_full + 8 * s, 2 * C::STAGE);
+            bulk_g2s_hint(sbase + s * C::STAGE, kbase + off, C::STAGE, bar_full + 8 * s, pol);
+            bulk_g2s_hint(sbase + (C::NSTAGE + s) * C::STAGE, vbase + off, C::STAGE,
                           bar_full + 8 * s, pol);
           }
         }
@@ -409,7 +423,8 @@ decode_paged_kernel(const DecodeArgs a) {
 
     const float beta2 = kUnifiedBeta * kLog2e;
     bool first_chunk = true;
-    for (int i = warp; i < n_pages; i += C::NW) {
+    // a head's WPH warps take its pages in turn; every stage is read by one warp per head
+    for (int i = warp % C::WPH; i < n_pages; i += C::WPH) {
       const int s = i % C::NSTAGE;
       if (!mbar_wait(bar_full + 8 * s, (i / C::NSTAGE) & 1)) {
         if (lane == 0) {
@@ -418,12 +433,12 @@ decode_paged_kernel(const DecodeArgs a) {
         }
         break;
       }
-      const KV* kt = reinterpret_cast<const KV*>(smem + s * C::TILE);
-      const KV* vt = reinterpret_cast<const KV*>(smem + (C::NSTAGE + s) * C::TILE);
-      // FP8: this stage's tile scales (1 otherwise; multiplied in only for FP8)
+      const KV* kt = reinterpret_cast<const KV*>(smem + s * C::STAGE + hh * C::TILE);
+      const KV* vt = reinterpret_cast<const KV*>(smem + (C::NSTAGE + s) * C::STAGE + hh * C::TILE);
+      // FP8: this stage's tile scales for the warp's head (1 otherwise; used only for FP8)
       float ks = 1.0f, vs = 1.0f;
       if constexpr (FP8) {
-        const float* scl = reinterpret_cast<const float*>(smem + C::SCALE_OFF) + 2 * s;
+        const float* scl = reinterpret_cast<const float*>(smem + C::SCALE_OFF) + 2 * (C::HPC * s + hh);
         ks = scl[0];
         vs = scl[1];
       }
@@ -713,10 +728,10 @@ decode_paged_kernel(const DecodeArgs a) {
     }
     __syncthreads();
     if (final_write) {
-      write_group_const<T, D, G>(a, b, g, NAN, NAN);
+      for (int k = 0; k < C::HPC; ++k) write_group_const<T, D, G>(a, b, g0 + k, NAN, NAN);
     } else {
-      for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const size_t row = (size_t)b * a.n_qo_heads + g * G + idx / D;
+      for (int idx = threadIdx.x; idx < C::HPC * G * D; idx += blockDim.x) {
+        const size_t row = (size_t)b * a.n_qo_heads + g0 * G + idx / D;
         a.part_o[(row * a.num_splits + split) * D + idx % D] = NAN;
         if (idx % D == 0) a.part_lse[row * a.num_splits + split] = NAN;
       }
@@ -762,15 +777,17 @@ decode_paged_kernel(const DecodeArgs a) {
     if (threadIdx.x == 0 && flags->fallbacks && a.fallback_count)
       atomicAdd(a.fallback_count, flags->fallbacks);
   }
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int gi = idx / D;
+  for (int idx = threadIdx.x; idx < C::HPC * G * D; idx += blockDim.x) {
+    const int hk = idx / (G * D);  // head within the CTA; its warps are hk*WPH ..
+    const int gi = (idx / D) % G;
     const int d = idx % D;
+    const int w0 = hk * C::WPH;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, cref[w * G + gi]);
+    for (int w = w0; w < w0 + C::WPH; ++w) M = fmaxf(M, cref[w * G + gi]);
     float L = 0.0f, O = 0.0f;
 #pragma unroll
-    for (int w = 0; w < C::NW; ++w) {
+    for (int w = w0; w < w0 + C::WPH; ++w) {
       const float f = ex2(cref[w * G + gi] - M);  // 0 for a warp that saw no page
       L = fmaf(f, cl[w * G + gi], L);
       O = fmaf(f, cacc[(w * G + gi) * D + d], O);
@@ -781,7 +798,7 @@ decode_paged_kernel(const DecodeArgs a) {
       O = NAN;
       lse = NAN;
     }
-    const int h = g * G + gi;
+    const int h = (g0 + hk) * G + gi;
     const size_t row = (size_t)b * a.n_qo_heads + h;
     if (final_write) {
       static_cast<T*>(a.out)[row * D + d] = from_f32<T>(O);
@@ -805,7 +822,7 @@ int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
       return PKV_ERR_LAUNCH;
     configured_mask |= (1 << dev);
   }
-  dim3 grid(a.num_splits, a.n_kv_heads, a.batch);
+  dim3 grid(a.num_splits, a.n_kv_heads / C::HPC, a.batch);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a);
   return check_launch(cudaGetLastError());
 }
