@@ -91,8 +91,10 @@ const char* attn_last_cuda_error_string(void);
  * Number of KV splits the decode calls use for this shape and dtype. num_splits > 0
  * is taken as asked (capped at max_blocks_per_seq); 0 lets the library choose from
  * the shape, the SM count of the current device and how many decode CTAs fit on an
- * SM, as the split count that minimises (waves of CTAs) x (pages per CTA + 4). A split covers a contiguous
- * range of ceil(max_blocks_per_seq / splits) pages of a sequence.
+ * SM, as the split count that minimises (waves of CTAs) x (pages per CTA + 4), plus 24
+ * for the split merge when there is more than one split (so small problems get one
+ * split and no merge launch). A split covers a contiguous range of
+ * ceil(max_blocks_per_seq / splits) pages of a sequence.
  * FlashDecoding computes each partial softmax independently and combines them
  * all at the end ("【FlashAttention-V4，非官方】FlashDecoding++", section 1).
  * Returns the split count (>= 1) or a negative PKV_ERR_* code.

@@ -33,8 +33,11 @@ SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requ
     S = requested < max_blocks ? requested : max_blocks;
   } else {
     // Model the time of a split count as (waves of CTAs) x (pages per CTA + a fixed
-    // per-CTA cost of about 4 pages), assuming every sequence is full length, and
-    // take the cheapest. This favours splits that fill whole waves of resident CTAs.
+    // per-CTA cost of about 4 pages), assuming every sequence is full length, plus the
+    // split merge when there is more than one split: one more launch, whose latency is
+    // worth about 24 pages of one CTA's streaming. Take the cheapest. This favours splits
+    // that fill whole waves of resident CTAs, and one split for small problems.
+    constexpr long kMergePages = 24;
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
     const long slots = (long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
@@ -45,7 +48,7 @@ SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requ
     for (int s = 1; s <= s_max; ++s) {
       const long pps = (max_blocks + s - 1) / s;
       const long waves = (units * s + slots - 1) / slots;
-      const long cost = waves * (pps + 4);
+      const long cost = waves * (pps + 4) + (s > 1 ? kMergePages : 0);
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         S = s;
