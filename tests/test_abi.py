@@ -120,3 +120,28 @@ def test_unsupported_shapes_are_reported(b):
     q = ctypes.c_void_p((1 << 20) + 4)
     assert L.attn_decode_paged(p, q, p, p, p, p, p, 1, 1, 1, 8, 8, 64, 16, 1.0, 1, b.PKV_F32,
                                None, 0, None, None) == b.PKV_ERR_INVALID_ARG
+
+
+def test_planner_gives_small_problems_one_split(b):
+    # 1 MiB of K/V: one split and no merge launch beats 16 one-page splits plus a merge
+    assert b.decode_num_splits(1, 16, 8, 8, 64, 16, 0, b.PKV_F32) == 1
+    # the Llama-7B batch still splits (it fills the GPU in a few waves)
+    assert b.decode_num_splits(16, 256, 32, 32, 128, 16, 0, b.PKV_BF16) > 1
+
+
+def test_fp8_arguments_rejected_before_launch(b):
+    L = b.lib
+    p = ctypes.c_void_p(1 << 20)
+    # missing scales
+    assert L.attn_decode_paged_fp8(p, p, p, None, p, p, p, p, None, 1, 4, 8, 8, 8, 128, 16, 0.1, 1,
+                                   None, 0, None, None) == b.PKV_ERR_INVALID_ARG
+    # an odd number of KV heads: the FP8 kernel takes two per CTA
+    assert L.attn_decode_paged_fp8(p, p, p, p, p, p, p, p, None, 1, 4, 8, 3, 3, 128, 16, 0.1, 1,
+                                   None, 0, None, None) == b.PKV_ERR_UNSUPPORTED
+    assert b.lib.attn_decode_num_splits(1, 4, 3, 3, 128, 16, 0, b.PKV_FP8_E4M3) == b.PKV_ERR_UNSUPPORTED
+    # head_dim 96 is not built
+    assert L.attn_decode_paged_fp8(p, p, p, p, p, p, p, p, None, 1, 4, 8, 8, 8, 96, 16, 0.1, 1,
+                                   None, 0, None, None) == b.PKV_ERR_UNSUPPORTED
+    # the FP8 workspace query matches the bf16 one (same fp32 partials)
+    assert b.decode_workspace_size(4, 64, 32, 8, 128, 16, 8, b.PKV_FP8_E4M3) == \
+        b.decode_workspace_size(4, 64, 32, 8, 128, 16, 8, b.PKV_BF16)
