@@ -1,6 +1,7 @@
 // Paged single-token decode kernel (sm_103a).
 //
-// One CTA per (KV split, KV head, sequence). A producer warp streams the
+// One CTA per (KV split, KV head, sequence); the FP8 variant's CTA takes two adjacent
+// KV heads (see DecodeCfg). A producer warp streams the
 // split's (page, KV head) tiles of K and V (page_size x head_dim contiguous
 // elements each) through the block table into a ring of shared-memory stages.
 // It uses one-dimensional bulk TMA copies that complete on an mbarrier.

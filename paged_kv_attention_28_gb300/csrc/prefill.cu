@@ -1,12 +1,15 @@
 // Causal prefill attention on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
-// Tiled FlashAttention ("快速注意力内核与算子融合", Q&A on FlashAttention): a CTA
-// owns two adjacent 128-row query tiles, A and B, of one (batch, head). It
-// walks the 128-key K/V tiles up to B's diagonal, each in two steps of 64 keys. For
+// Tiled FlashAttention ("快速注意力内核与算子融合", Q&A on FlashAttention): a work
+// item is two adjacent 128-row query tiles, A and B, of one (batch, head). A CTA
+// walks the item's 128-key K/V tiles up to B's diagonal, each in two steps of 64 keys. For
 // each step it computes S = Q K^T into tensor memory, updates the running row max and
 // sum, writes P = exp(S - m) back into tensor memory as bf16, and accumulates O += P V
 // in tensor memory. The T x T score matrix never leaves the chip. The causal mask is
 // applied by predication on the two diagonal tiles only.
+//
+// The grid has one CTA per item; a running CTA also takes the items of CTAs that have
+// not started yet (cluster launch control, below), so one CTA per SM runs to the end.
 //
 // A and B share every K/V tile that TMA brings in. Each query tile has two S buffers,
 // so S for step s + 1 is computed while the softmax turns S_s into P_s: the chain
@@ -36,7 +39,7 @@
 // ("cascade") kernel. There a 128-row query tile is 128/G requests x the G query
 // heads of one KV head, and K/V tiles are gathered 16 rows (one page) at a time
 // through the prefix block table. The prefix is cut into chunks of key tiles,
-// one chunk per CTA, and each CTA writes fp32 partial (O, LSE) states that a
+// one chunk per item, and each item writes fp32 partial (O, LSE) states that a
 // later merge combines with the per-request suffix.
 #include <cuda.h>
 #include <cuda_bf16.h>
