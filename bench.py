@@ -433,7 +433,7 @@ def run_ours(args, rank, world, local):
                      "traffic": traffic, "kernel": "decode_paged_kernel (+ merge_splits_kernel inside the same events)"},
         "e2e_pipelined": {"value": pipe_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                           "d2h_bytes_per_step": d2h,
-                          "note": "the e2e steps with step i+1's inputs copied in on one stream and step i's results copied out on another while step i computes; two sets of packed buffers"},
+                          "note": "the e2e steps with step i+1's inputs copied in on one stream and step i's results copied out on another while step i computes; two sets of packed buffers; like the serial e2e, no L2 flush between steps (the 682 MB of K/V exceed the L2), and back-to-back steps hide each other's launch gaps"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "q, block_table and kv_lens copied in from one pinned host buffer and out, lse copied back into another, one copy each way every step; the KV page pool is resident device state"},
         "clocks": clocks,
