@@ -38,6 +38,11 @@ Readings where the pages are silent (the design document lists them too):
   Split ``s`` holds blocks ``[s*pps, (s+1)*pps)``.
 * The unified-max partial of a chunk is ``(sum exp(s - phi) v, sum exp(s - phi))``
   with a preset ``phi``. Chunks that share ``phi`` merge by plain sums.
+* A chunked prefill over a paged cache appends ``C`` new tokens to a sequence
+  that already holds ``L0`` tokens: the new tokens' K and V are in the cache at
+  positions ``L0 .. L0 + C - 1`` (written before the call), and new token ``i``
+  (position ``L0 + i``) sees keys ``0 .. L0 + i``. It joins the paged gather and
+  the causal mask; the pages describe both but not their combination.
 * FP8 pages hold E4M3 codes (the OCP 8-bit floating-point format), and each
   (page, KV head) tile of K and of V has one float scale: the element's value is
   ``e4m3(code) * scale``. Attention over FP8 pages is the plain attention over
@@ -53,7 +58,7 @@ __all__ = [
     "attend", "gather_sequence", "decode_paged", "prefill_causal", "merge_states",
     "merge_many", "split_ranges", "decode_split_partials", "cascade_decode",
     "unified_max_partials", "unified_max_combine", "unified_max_needs_fallback",
-    "e4m3_to_float", "decode_paged_fp8",
+    "e4m3_to_float", "decode_paged_fp8", "prefill_paged_chunk",
 ]
 
 NEG_INF = -math.inf
@@ -224,6 +229,34 @@ def prefill_causal(q, k, v, scale, rows=None):
         o, l = attend(q[b, i:i + 1, h], k[b, :i + 1, h // G], v[b, :i + 1, h // G], scale)
         out[b, i, h] = o[0]
         lse[b, h, i] = l[0]
+    return out, lse
+
+
+def prefill_paged_chunk(q, k_pages, v_pages, block_table, prefix_lens, scale):
+    """Chunked prefill over a paged cache.
+
+    ``q[B, C, Hq, D]`` holds the queries of ``C`` new tokens per sequence; sequence ``b``
+    already had ``prefix_lens[b]`` tokens, and its ``prefix_lens[b] + C`` tokens (old and
+    new) are in the pools ``[num_pages, Hkv, P, D]`` through ``block_table[b]``. New token
+    ``i`` attends to keys ``0 .. prefix_lens[b] + i``. Returns ``out[B, C, Hq, D]`` and
+    ``lse[B, Hq, C]``.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, C, Hq, D = q.shape
+    Hkv = k_pages.shape[1]
+    G = Hq // Hkv
+    out = np.full((B, C, Hq, D), np.nan)
+    lse = np.full((B, Hq, C), np.nan)
+    for b in range(B):
+        L0 = int(prefix_lens[b])
+        L = L0 + C
+        keep = np.arange(L)[None, :] <= (L0 + np.arange(C))[:, None]   # [C, L]
+        for g in range(Hkv):
+            K, V = _gather_fast(k_pages, v_pages, block_table[b], L, g)
+            for h in range(g * G, (g + 1) * G):
+                o, l = attend(q[b, :, h], K, V, scale, keep=keep)
+                out[b, :, h] = o
+                lse[b, h] = l
     return out, lse
 
 

@@ -796,3 +796,132 @@ def test_e4m3_planted_mistakes_are_caught(kind):
 @pytest.mark.parametrize("kind", ["scale_transposed", "k_scale_for_v", "page_not_logical"])
 def test_fp8_decode_planted_mistakes_are_caught(kind):
     assert not all(pin(_fp8_decode_mutant(kind)) for pin in FP8_DECODE_PINS)
+
+
+# ----------------------------------------------------------------------------- chunked paged prefill
+
+def _chunk_case(seed, B=2, C=5, Hq=4, Hkv=2, D=8, P=4, prefix=(7, 0), n_pages=16):
+    r = np.random.default_rng(seed)
+    L = [L0 + C for L0 in prefix]
+    nblk = [(l + P - 1) // P for l in L]
+    order = r.permutation(n_pages)
+    table = np.full((B, max(nblk)), -1)
+    pos = 0
+    for b in range(B):
+        table[b, :nblk[b]] = order[pos:pos + nblk[b]]
+        pos += nblk[b]
+    # the sequences' K and V, contiguous, then scattered into the pool through the table
+    ks = [r.normal(size=(l, Hkv, D)) for l in L]
+    vs = [r.normal(size=(l, Hkv, D)) for l in L]
+    kp = np.full((n_pages, Hkv, P, D), np.nan)
+    vp = np.full((n_pages, Hkv, P, D), np.nan)
+    for b in range(B):
+        for t in range(L[b]):
+            kp[table[b, t // P], :, t % P] = ks[b][t]
+            vp[table[b, t // P], :, t % P] = vs[b][t]
+    q = r.normal(size=(B, C, Hq, D))
+    return q, kp, vp, table, np.array(prefix), ks, vs, 0.4
+
+
+def check_chunk_without_prefix_is_causal_prefill(f):
+    q, kp, vp, table, _, ks, vs, scale = _chunk_case(21, prefix=(0, 0))
+    got = f(q, kp, vp, table, np.array([0, 0]), scale)
+    want = oracle.prefill_causal(q, np.stack(ks), np.stack(vs), scale)
+    return np.allclose(got[0], want[0], atol=1e-12) and np.allclose(got[1], want[1], atol=1e-12)
+
+
+def check_single_token_chunk_is_decode(f):
+    q, kp, vp, table, prefix, ks, vs, scale = _chunk_case(22, C=1, prefix=(9, 3))
+    got = f(q, kp, vp, table, prefix, scale)
+    want = oracle.decode_paged(q[:, 0], kp, vp, table, prefix + 1, scale)
+    return np.allclose(got[0][:, 0], want[0], atol=1e-12) and np.allclose(got[1][:, :, 0], want[1], atol=1e-12)
+
+
+def check_chunks_compose(f):
+    # one chunk of 5 new tokens = a chunk of 2 followed by a chunk of 3
+    q, kp, vp, table, prefix, ks, vs, scale = _chunk_case(23, C=5, prefix=(6, 1))
+    whole = f(q, kp, vp, table, prefix, scale)
+    first = f(q[:, :2], kp, vp, table, prefix, scale)
+    second = f(q[:, 2:], kp, vp, table, prefix + 2, scale)
+    return (np.allclose(whole[0][:, :2], first[0], atol=1e-12) and np.allclose(whole[0][:, 2:], second[0], atol=1e-12)
+            and np.allclose(whole[1][:, :, :2], first[1], atol=1e-12) and np.allclose(whole[1][:, :, 2:], second[1], atol=1e-12))
+
+
+def check_chunk_brute_force(f):
+    q, kp, vp, table, prefix, ks, vs, scale = _chunk_case(24, B=1, C=3, Hq=2, Hkv=1, D=3, prefix=(4,))
+    got = f(q, kp, vp, table, prefix, scale)
+    L0 = int(prefix[0])
+    for i in range(3):
+        for h in range(2):
+            sc = [scale * math.fsum(q[0, i, h, d] * ks[0][j][0][d] for d in range(3)) for j in range(L0 + i + 1)]
+            m = max(sc)
+            w = [math.exp(x - m) for x in sc]
+            z = math.fsum(w)
+            o = [math.fsum(w[j] * vs[0][j][0][d] for j in range(len(w))) / z for d in range(3)]
+            if not (np.allclose(got[0][0, i, h], o, atol=1e-12) and abs(got[1][0, h, i] - (m + math.log(z))) < 1e-12):
+                return False
+    return True
+
+
+def check_chunk_page_shuffle(f):
+    q, kp, vp, table, prefix, ks, vs, scale = _chunk_case(25)
+    perm = np.random.default_rng(5).permutation(kp.shape[0])
+    kp2 = np.empty_like(kp)
+    vp2 = np.empty_like(vp)
+    kp2[perm] = kp
+    vp2[perm] = vp
+    table2 = np.where(table >= 0, perm[np.maximum(table, 0)], -1)
+    a = f(q, kp, vp, table, prefix, scale)
+    b2 = f(q, kp2, vp2, table2, prefix, scale)
+    return np.allclose(a[0], b2[0], atol=1e-13) and np.allclose(a[1], b2[1], atol=1e-13)
+
+
+CHUNK_PINS = [check_chunk_without_prefix_is_causal_prefill, check_single_token_chunk_is_decode,
+              check_chunks_compose, check_chunk_brute_force, check_chunk_page_shuffle]
+
+
+@pytest.mark.parametrize("pin", CHUNK_PINS)
+def test_prefill_paged_chunk_pins(pin):
+    assert pin(oracle.prefill_paged_chunk)
+
+
+def _chunk_mutant(kind):
+    def f(q, kp, vp, table, prefix, scale):
+        q = np.asarray(q, dtype=np.float64)
+        B, C, Hq, D = q.shape
+        Hkv = kp.shape[1]
+        G = Hq // Hkv
+        P = kp.shape[2]
+        out = np.full((B, C, Hq, D), np.nan)
+        lse = np.full((B, Hq, C), np.nan)
+        for b in range(B):
+            L0 = int(prefix[b])
+            L = L0 + C
+            lim = (L0 + np.arange(C)) if kind != "no_offset" else np.arange(C)
+            keep = (np.arange(L)[None, :] < lim[:, None]) if kind == "strict" else (np.arange(L)[None, :] <= lim[:, None])
+            tb = table[0] if kind == "first_table" else table[b]
+            t = np.arange(L)
+            pages = np.asarray(tb)[t // P]
+            for h in range(Hq):
+                g = h % Hkv if kind == "gqa_modulo" else h // G
+                K = kp[pages, g, t % P]
+                V = vp[pages, g, t % P]
+                o, l = oracle.attend(q[b, :, h], K, V, scale, keep=keep)
+                out[b, :, h] = o
+                lse[b, h] = l
+        return out, lse
+    return f
+
+
+@pytest.mark.parametrize("kind", ["strict", "no_offset", "first_table", "gqa_modulo"])
+def test_prefill_paged_chunk_planted_mistakes_are_caught(kind):
+    failed = []
+    for pin in CHUNK_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                ok = pin(_chunk_mutant(kind))
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {kind} passed every pin"
