@@ -563,6 +563,28 @@ def other_workloads(B, workloads, dev, stream, steps, hbm_peak):
           {"bytes_note": "shared prefix K/V counted once plus every suffix"})
     del q, kp, vp, pt, st, sl, ws
 
+    # Chunked prefill over the paged cache: 8 sequences of Llama-7B heads, each appending
+    # 1024 tokens to a 3072-token prefix (the new tokens' K/V already in the pages).
+    n_seq, C, L0 = 8, 1024, 3072
+    c = workloads.make_paged_decode(1006, n_seq, 32, 32, 128, 16, [L0 + C] * n_seq, dtype="bf16",
+                                    poison=False)
+    gen = torch.Generator().manual_seed(1007)
+    qc = torch.randn((n_seq, C, 32, 128), generator=gen, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    kp, vp, bt = c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev)
+    pl = torch.full((n_seq,), L0, dtype=torch.int32, device=dev)
+    out = torch.empty_like(qc)
+    lse = torch.empty((n_seq, 32, C), dtype=torch.float32, device=dev)
+    ms = time_calls(lambda: B.prefill_paged_chunk(qc, kp, vp, bt, pl, c.scale, out=out, lse=lse),
+                    steps, stream, dev)
+    flops = 4 * 128 * 32 * n_seq * (C * L0 + C * (C + 1) // 2)
+    tf = flops / (ms / 1e3) / 1e12
+    res["chunked_prefill_paged"] = {
+        "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "flops": flops,
+        "frac_of_measured_bf16": tf / peaks()[1],
+        "workload": f"{n_seq} sequences x {C} new tokens after a {L0}-token prefix, 32/32 heads, d 128, "
+                    "page 16, bf16 (attended pairs only)"}
+    del qc, kp, vp, bt, pl, out, lse
+
     c = workloads.single_seq_decode_f32()
     q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
     ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale), steps, stream, dev)

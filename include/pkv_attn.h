@@ -223,6 +223,31 @@ int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_page
                           void* stream);
 
 /*
+ * Chunked prefill over the paged cache: each sequence b already holds prefix_lens[b]
+ * tokens and appends chunk_len new ones, whose K and V the caller has already written
+ * into the pages at positions prefix_lens[b] .. prefix_lens[b] + chunk_len - 1. New
+ * token i attends to keys 0 .. prefix_lens[b] + i of its own sequence (the causal mask
+ * with an offset), read through the block table ("快速注意力内核与算子融合", Q&A on
+ * paged attention and on FlashAttention; the pages do not describe the combination).
+ *
+ *   q, out      : bf16 [batch][chunk_len][n_qo_heads][head_dim], contiguous
+ *   k_pages, v_pages, block_table : the paged layout above (bf16 pools)
+ *   prefix_lens : int32 [batch]; prefix_lens[b] + chunk_len must fit the table's
+ *                 max_blocks_per_seq pages (else PKV_DEVERR_BAD_LEN, computed on a
+ *                 clamped length)
+ *   lse         : fp32 [batch][n_qo_heads][chunk_len] (nullable)
+ * Both products run on the tcgen05 tensor cores (the prefill kernel's paged mode). Built
+ * for bf16, head_dim 128, page_size 16 and GQA groups dividing 128; all pointers 16-byte
+ * aligned.
+ */
+int attn_prefill_paged_chunk(const void* q, const void* k_pages, const void* v_pages,
+                             const int32_t* block_table, const int32_t* prefix_lens, void* out,
+                             float* lse, int batch, int chunk_len, int max_blocks_per_seq,
+                             int num_pages, int n_qo_heads, int n_kv_heads, int head_dim,
+                             int page_size, float scale, int dtype, int32_t* err_flag,
+                             void* stream);
+
+/*
  * Merge two partial softmax states over disjoint key sets into one
  * ("【FlashAttention-V4，非官方】FlashDecoding++", section 1: partial softmax
  * results are updated at the end):

@@ -33,7 +33,7 @@ EXPORTS = [
     "attn_status_string", "attn_last_cuda_error_string", "attn_decode_num_splits", "attn_decode_workspace_size",
     "attn_decode_paged", "attn_decode_paged_unified_max", "attn_merge_states",
     "attn_prefill_causal", "attn_cascade_workspace_size", "attn_decode_cascade",
-    "attn_decode_paged_noalloc", "attn_decode_paged_fp8",
+    "attn_decode_paged_noalloc", "attn_decode_paged_fp8", "attn_prefill_paged_chunk",
 ]
 
 
@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_merge_states.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, vp]
     lib.attn_prefill_causal.restype = i32
     lib.attn_prefill_causal.argtypes = [vp, vp, vp, vp, vp] + [i32] * 5 + [f32, i32, vp, vp]
+    lib.attn_prefill_paged_chunk.restype = i32
+    lib.attn_prefill_paged_chunk.argtypes = [vp] * 7 + [i32] * 8 + [f32, i32, vp, vp]
     lib.attn_cascade_workspace_size.restype = sz
     lib.attn_cascade_workspace_size.argtypes = [i32] * 7
     lib.attn_decode_cascade.restype = i32
@@ -251,6 +253,33 @@ def prefill_causal(q, k, v, scale, out=None, lse=None, err_flag=None, stream=Non
     st = lib.attn_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, T, Hq, Hkv, D,
                                  float(scale), _dt(q), _ptr(err_flag), _stream(stream))
     _check(st, "attn_prefill_causal")
+    return out, lse
+
+
+def prefill_paged_chunk(q, k_pages, v_pages, block_table, prefix_lens, scale, out=None, lse=None,
+                        err_flag=None, stream=None):
+    """Chunked prefill over the paged cache through ``attn_prefill_paged_chunk``.
+
+    ``q`` ``[B, C, Hq, D]``; the new tokens' K/V are already in the pools. Returns
+    ``(out, lse)`` with ``lse`` ``[B, Hq, C]``."""
+    B, C, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = k_pages.shape
+    assert D2 == D
+    max_blocks = block_table.shape[1]
+    _need(q, "q")
+    _need(k_pages, "k_pages", q.dtype)
+    _need(v_pages, "v_pages", q.dtype, k_pages.shape)
+    _need(block_table, "block_table", torch.int32, (B, max_blocks))
+    _need(prefix_lens, "prefix_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, C), dtype=torch.float32, device=q.device)
+    st = lib.attn_prefill_paged_chunk(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(block_table),
+                                      _ptr(prefix_lens), _ptr(out), _ptr(lse), B, C, max_blocks,
+                                      num_pages, Hq, Hkv, D, P, float(scale), _dt(q), _ptr(err_flag),
+                                      _stream(stream))
+    _check(st, "attn_prefill_paged_chunk")
     return out, lse
 
 

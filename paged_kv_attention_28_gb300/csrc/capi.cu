@@ -260,6 +260,31 @@ int attn_prefill_causal(const void* q, const void* k, const void* v, void* out, 
   return launch_prefill(a, static_cast<cudaStream_t>(stream));
 }
 
+int attn_prefill_paged_chunk(const void* q, const void* k_pages, const void* v_pages,
+                             const int32_t* block_table, const int32_t* prefix_lens, void* out,
+                             float* lse, int batch, int chunk_len, int max_blocks_per_seq,
+                             int num_pages, int n_qo_heads, int n_kv_heads, int head_dim,
+                             int page_size, float scale, int dtype, int32_t* err_flag,
+                             void* stream) {
+  if (batch < 0 || chunk_len < 0 || max_blocks_per_seq < 1 || num_pages < 1 || n_qo_heads < 1 ||
+      n_kv_heads < 1 || head_dim < 1 || page_size < 1)
+    return PKV_ERR_INVALID_ARG;
+  if (n_qo_heads % n_kv_heads || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if ((long)max_blocks_per_seq * page_size > 0x7fffffffL) return PKV_ERR_INVALID_ARG;
+  if (chunk_len > max_blocks_per_seq * page_size) return PKV_ERR_INVALID_ARG;
+  if (batch == 0 || chunk_len == 0) return PKV_OK;
+  if (!q || !k_pages || !v_pages || !block_table || !prefix_lens || !out) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return PKV_ERR_INVALID_ARG;
+  const int G = n_qo_heads / n_kv_heads;
+  if (dtype != PKV_BF16 || head_dim != 128 || page_size != 16 || 128 % G) return PKV_ERR_UNSUPPORTED;
+  if (batch > 65535) return PKV_ERR_UNSUPPORTED;
+  ChunkArgs a{q, k_pages, v_pages, block_table, prefix_lens, out, lse, err_flag, batch, chunk_len,
+              max_blocks_per_seq, num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale};
+  return launch_prefill_chunk(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t attn_cascade_workspace_size(int n_requests, int prefix_len, int max_suffix_blocks,
                                    int n_qo_heads, int n_kv_heads, int head_dim, int page_size) {
   if (n_requests < 0 || prefix_len < 0 || max_suffix_blocks < 1 || n_qo_heads < 1 ||

@@ -105,6 +105,20 @@ int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_q
 SplitPlan cascade_suffix_plan(int n_requests, int max_suffix_blocks, int n_qo_heads,
                               int n_kv_heads, int head_dim, int dtype);
 int launch_cascade_prefix(const CascadeArgs& a, cudaStream_t stream);
+
+struct ChunkArgs {
+  const void* q;        // bf16 [batch][chunk_len][n_qo_heads][head_dim]
+  const void* k_pages;  // bf16 [num_pages][n_kv_heads][page_size][head_dim]
+  const void* v_pages;
+  const int32_t* block_table;  // [batch][max_blocks]
+  const int32_t* prefix_lens;  // [batch]
+  void* out;                   // bf16 [batch][chunk_len][n_qo_heads][head_dim]
+  float* lse;                  // fp32 [batch][n_qo_heads][chunk_len] (nullable)
+  int32_t* err_flag;
+  int batch, chunk_len, max_blocks, num_pages, n_qo_heads, n_kv_heads, head_dim, page_size;
+  float scale;
+};
+int launch_prefill_chunk(const ChunkArgs& a, cudaStream_t stream);
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream);
 
 }  // namespace pkv

@@ -111,6 +111,10 @@ struct TileArgs {
   int tiles_per_chunk, n_chunks, n_row_pairs;
   float* part_o;      // fp32 [n_chunks][n_requests][Hq][D]
   float* part_lse;    // fp32 [n_chunks][n_requests][Hq]
+  // chunked prefill over the paged cache: C new tokens per sequence after prefix_lens[b]
+  const int32_t* block_table;  // int32 [batch][max_blocks]
+  const int32_t* prefix_lens;  // int32 [batch]
+  int chunk_len, max_blocks;
 };
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -217,6 +221,9 @@ struct TileJob {
   int q0, b, h;
   // prefix: row r of the tile is request r0 + r / G, query head g*G + r % G, chunk c
   int r0, g, c;
+  // chunk: row r is new token q0 + r / G (position L0 + q0 + r / G) of sequence b, query
+  // head g*G + r % G
+  int L0;
 };
 
 // One work item: two query tiles (A, B) that share their key tiles.
@@ -229,12 +236,38 @@ struct Item {
   int b;         // causal: batch
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool CHUNK = false>
 __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
   Item it{};
   const int H = a.n_qo_heads;
   const int G = a.n_qo_heads / a.n_kv_heads;
-  if constexpr (CAUSAL) {
+  if constexpr (CHUNK) {
+    // Items (query-tile pair, KV head, sequence), the pairs with the most key tiles first.
+    // A tile is 128/G new tokens x the G query heads of one KV head.
+    const int TPT = BM / G;  // tokens per tile
+    const int n_qt = (a.chunk_len + TPT - 1) / TPT;
+    const int n_pairs = (n_qt + 1) / 2;
+    const int per_pr = a.batch * a.n_kv_heads;
+    const int pr = n_pairs - 1 - id / per_pr;
+    const int rem = id % per_pr;
+    const int hk = rem % a.n_kv_heads;
+    const int b = rem / a.n_kv_heads;
+    int L0 = __ldg(a.prefix_lens + b);
+    const int cap = a.max_blocks * 16 - a.chunk_len;
+    if (L0 < 0 || L0 > cap) {  // reported; the rows are then computed on a clamped length
+      set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
+      L0 = L0 < 0 ? 0 : cap;
+    }
+    const int q0A = 2 * pr * TPT, q0B = q0A + TPT;
+    const bool has_b = q0B < a.chunk_len;
+    // key tiles up to the last real token of the tile (position L0 + last)
+    auto tiles = [&](int q0) { return (L0 + min(q0 + TPT, a.chunk_len) + BN - 1) / BN; };
+    it.hk = hk;
+    it.b = b;
+    it.A = TileJob{tiles(q0A), 0, q0A, b, 0, 0, hk, 0, L0};
+    it.B = TileJob{has_b ? tiles(q0B) : 0, 0, q0B, b, 0, 0, hk, 0, L0};
+    it.n_kv = has_b ? it.B.n_tiles : it.A.n_tiles;
+  } else if constexpr (CAUSAL) {
     const int n_qt = (a.seq_len + BM - 1) / BM;
     const int n_pairs = (n_qt + 1) / 2;
     // Longest first: the pairs nearest the end of the sequence have the most key tiles.
@@ -267,8 +300,8 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
     it.b = b;
     it.n_kv = has_b ? qtA + 2 : qtA + 1;
     it.qrow = qtA * BM;
-    it.A = TileJob{qtA + 1, BN, qtA * BM, b, h, 0, 0, 0};
-    it.B = TileJob{has_b ? qtA + 2 : 0, BN, (qtA + 1) * BM, b, h, 0, 0, 0};
+    it.A = TileJob{qtA + 1, BN, qtA * BM, b, h, 0, 0, 0, 0};
+    it.B = TileJob{has_b ? qtA + 2 : 0, BN, (qtA + 1) * BM, b, h, 0, 0, 0, 0};
   } else {
     const int c = id % a.n_chunks;
     const int rest = id / a.n_chunks;
@@ -281,8 +314,8 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
     const bool has_b = (pr * 2 * BM + BM) < a.n_requests * G;
     it.qrow = pr * 2 * BM;
     const int last_valid = a.prefix_len - (it.kv_first + it.n_kv - 1) * BN;
-    it.A = TileJob{it.n_kv, last_valid, 0, 0, 0, it.qrow / G, hk, c};
-    it.B = TileJob{has_b ? it.n_kv : 0, last_valid, 0, 0, 0, (it.qrow + BM) / G, hk, c};
+    it.A = TileJob{it.n_kv, last_valid, 0, 0, 0, it.qrow / G, hk, c, 0};
+    it.B = TileJob{has_b ? it.n_kv : 0, last_valid, 0, 0, 0, (it.qrow + BM) / G, hk, c, 0};
   }
   return it;
 }
@@ -290,7 +323,7 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
 // The softmax warpgroup of one query tile of every item of this CTA: S -> P for each
 // 64-key step, then the hand-off to the epilogue. Step g of the tile (counted across
 // items) uses S buffer g & 1 and barriers s_full[g & 1], p_full[g & 1].
-template <bool CAUSAL>
+template <bool CAUSAL, bool CHUNK = false>
 __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint32_t bar_sf0,
                                              uint32_t bar_pf0, uint32_t bar_od, uint32_t bar_st,
                                              uint32_t bar_ie, float* inv_rows,
@@ -307,7 +340,7 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
   bool ok = true;
   uint32_t k = 0;
   for (int id = blockIdx.x; id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
-    const Item it = make_item<CAUSAL>(a, id);
+    const Item it = make_item<CAUSAL, CHUNK>(a, id);
     const TileJob& job = tile == 0 ? it.A : it.B;
     const int n_steps = 2 * job.n_tiles;
     if (n_steps == 0) continue;
@@ -324,7 +357,17 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
       tmem_ld32(tSb + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_ld_wait();
       float* x = reinterpret_cast<float*>(sr);
-      if (s >= n_steps - 2) {
+      if constexpr (CHUNK) {
+        // row r (position L0 + q0 + r/G) sees keys up to its own position; the step holds
+        // keys [64 s, 64 s + 64)
+        const int first_pos = job.L0 + job.q0;  // the tile's smallest position
+        if (s * BS + BS > first_pos + 1) {
+          const int G = a.n_qo_heads / a.n_kv_heads;
+          const int limit = first_pos + r / G + 1 - s * BS;
+#pragma unroll
+          for (int i = 0; i < BS; ++i) x[i] = (i >= limit) ? -INFINITY : x[i];
+        }
+      } else if (s >= n_steps - 2) {
         // causal: key column k of the tile is visible to row r iff k <= r (diagonal
         // tile); prefix: only the first last_valid keys of the last tile exist
         const int limit = (CAUSAL ? r + 1 : job.last_valid) - (s & 1) * BS;
@@ -401,7 +444,12 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
     if (!ok && lane == 0) fail(misc, a.err_flag);
     if (*reinterpret_cast<volatile int*>(&misc->bad_page)) ok = false;
     const float lse_row = ok ? (ms + log2f(l)) * kLn2F : NAN;
-    if constexpr (CAUSAL) {
+    if constexpr (CHUNK) {
+      const int G = a.n_qo_heads / a.n_kv_heads;
+      const int t = job.q0 + r / G;
+      if (t < a.chunk_len && a.lse)
+        a.lse[((size_t)job.b * H + job.g * G + r % G) * a.chunk_len + t] = lse_row;
+    } else if constexpr (CAUSAL) {
       const int t = job.q0 + r;
       if (t < a.seq_len && a.lse) a.lse[((size_t)job.b * H + job.h) * a.seq_len + t] = lse_row;
     } else {
@@ -419,7 +467,7 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
 
 // The epilogue warpgroup: for each item and each of its query tiles, waits for the
 // tile's 1/l and its last PV, then writes O / l to global memory and frees O.
-template <bool CAUSAL>
+template <bool CAUSAL, bool CHUNK = false>
 __device__ __forceinline__ void epilogue_loop(const TileArgs& a, Misc* misc, uint32_t (&bars)[8],
                                               const float* inv_rows_base, int n_items,
                                               const NextRing& ring, int warp, int lane) {
@@ -431,7 +479,7 @@ __device__ __forceinline__ void epilogue_loop(const TileArgs& a, Misc* misc, uin
   bool ok = true;
   uint32_t k = 0;
   for (int id = blockIdx.x; id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
-    const Item it = make_item<CAUSAL>(a, id);
+    const Item it = make_item<CAUSAL, CHUNK>(a, id);
     for (int t = 0; t < 2; ++t) {
       const TileJob& job = t == 0 ? it.A : it.B;
       if (job.n_tiles == 0) continue;
@@ -446,11 +494,16 @@ __device__ __forceinline__ void epilogue_loop(const TileArgs& a, Misc* misc, uin
       const float inv = ok ? inv_rows_base[t * BM + r] : NAN;
       mbar_arrive(bar_ie);  // the softmax may write this tile's next 1/l
       const uint32_t tO = misc->tmem_base + lane_addr + COL_O + t * HD;
-      if constexpr (CAUSAL) {
-        const int tt = job.q0 + r;
-        const bool store = tt < a.seq_len;  // rows past a ragged end are computed but not stored
+      if constexpr (CAUSAL || CHUNK) {
+        // causal: row r is token q0 + r of head h; chunk: new token q0 + r/G of query head
+        // g*G + r%G. Rows past a ragged end are computed but not stored.
+        const int G = a.n_qo_heads / a.n_kv_heads;
+        const int tt = CHUNK ? job.q0 + r / G : job.q0 + r;
+        const int hh = CHUNK ? job.g * G + r % G : job.h;
+        const int T = CHUNK ? a.chunk_len : a.seq_len;
+        const bool store = tt < T;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
-                                              (((size_t)job.b * a.seq_len + tt) * H + job.h) * HD);
+                                              (((size_t)job.b * T + (store ? tt : 0)) * H + hh) * HD);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t o[32];
@@ -499,7 +552,7 @@ __device__ __forceinline__ void epilogue_loop(const TileArgs& a, Misc* misc, uin
 
 // One CTA per item in the grid; a running CTA also takes the items of CTAs that have
 // not started yet (work distribution above), so one CTA per SM runs to the end.
-template <bool CAUSAL>
+template <bool CAUSAL, bool CHUNK = false>
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const TileArgs a, int n_items) {
@@ -579,10 +632,14 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             tma_load_4d(dst + SUB, map, 64, it.hk, k0, it.b, full);
           } else {
             // Eight pages of 16 keys make one 128-key tile; each page is a 16-row box.
-            // Slots past the prefix reload its first page (finite data; masked out).
+            // Slots past the prefix (or the sequence) reload its first page (finite data;
+            // masked out).
+            // chunk: the sequence's own pages, up to its last new token
+            const int n_seq_pages = CHUNK ? (it.A.L0 + a.chunk_len + 15) / 16 : a.n_prefix_pages;
+            const int32_t* table = CHUNK ? a.block_table + (size_t)it.b * a.max_blocks : a.prefix_table;
             for (int pp = 0; pp < 8; ++pp) {
               const int page_idx = (it.kv_first + j) * 8 + pp;
-              int phys = __ldg(a.prefix_table + (page_idx < a.n_prefix_pages ? page_idx : 0));
+              int phys = __ldg(table + (page_idx < n_seq_pages ? page_idx : 0));
               if (phys < 0 || phys >= a.num_pages) {
                 misc->bad_page = 1;
                 set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
@@ -598,7 +655,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         };
         uint32_t k = 0, n_req = 0;
         for (int id = blockIdx.x; ok && id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
-          const Item it = make_item<CAUSAL>(a, id);
+          const Item it = make_item<CAUSAL, CHUNK>(a, id);
           // Q_t may be replaced once the previous item's last S_t has read it.
           auto load_q = [&](int t) -> bool {
             const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
@@ -607,7 +664,9 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
               mbar_arrive_expect_tx(qf, TILE);
               for (int half = 0; half < 2; ++half) {
                 const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
-                if constexpr (CAUSAL)
+                if constexpr (CHUNK)
+                  tma_load_4d(dst, &mq, half * 64, it.hk * G, (t == 0 ? it.A : it.B).q0, it.b, qf);
+                else if constexpr (CAUSAL)
                   tma_load_4d(dst, &mq, half * 64, it.A.h, it.qrow + t * BM, it.b, qf);
                 else
                   tma_load_3d(dst, &mq, half * 64, it.hk * G, (it.qrow + t * BM) / G, qf);
@@ -708,7 +767,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         bool ok = true;
         uint32_t k = 0;
         for (int id = blockIdx.x; ok && id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
-          const Item it = make_item<CAUSAL>(a, id);
+          const Item it = make_item<CAUSAL, CHUNK>(a, id);
           const int n_t = (t == 0 ? it.A : it.B).n_tiles;  // key tiles this tile reads
           const int n_o = (t == 0 ? it.B : it.A).n_tiles;  // key tiles the other tile reads
           const int n_kv = it.n_kv;
@@ -745,6 +804,23 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             }
             const uint32_t vg = v_cnt + j;
             if (half == 0 && !warp_wait(bar(BAR_VF + vg % NSV), (vg / NSV) & 1)) { ok = false; break; }
+            if constexpr (CHUNK) {
+              // The tile holding the sequence's last key also holds page slots past it,
+              // whose contents are not the caller's data (they may not even be finite): zero
+              // those V rows, since a masked key still enters PV as 0 x V. Both issuers may
+              // write the same zeros; each makes its writes visible to the tensor core first.
+              const int pos_end = it.A.L0 + a.chunk_len;  // keys [0, pos_end) exist
+              if (half == 0 && j == (pos_end - 1) / BN) {
+                unsigned char* vt = smem + SM_V + (vg % NSV) * TILE;
+                for (int row = pos_end - j * BN + (lane >> 3); row < BN; row += 4)
+#pragma unroll
+                  for (int sub = 0; sub < 2; ++sub)
+                    *reinterpret_cast<uint4*>(vt + sub * SUB + row * 128 + (lane & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+              }
+            }
             tc_fence_after();
             issue_pv(g, vg, half, st == 0, half == 1 ? rel(j) : 0, st == n_s - 1);
             // S two steps ahead reuses P_g's buffer: the in-order tensor pipe reads P_g first.
@@ -770,7 +846,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
     const int t = (warp - 4) / 4;
-    softmax_loop<CAUSAL>(a, misc, bar(BAR_SF + 2 * t), bar(BAR_PF + 2 * t), bar(BAR_OD + t),
+    softmax_loop<CAUSAL, CHUNK>(a, misc, bar(BAR_SF + 2 * t), bar(BAR_PF + 2 * t), bar(BAR_OD + t),
                          bar(BAR_ST + t), bar(BAR_IE + t),
                          reinterpret_cast<float*>(smem + SM_INV) + t * BM, COL_S + t * BN,
                          COL_O + t * HD, t, n_items, ring, warp, lane);
@@ -778,7 +854,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
     uint32_t bars[8] = {bar(BAR_ST), bar(BAR_ST + 1), bar(BAR_OI),     bar(BAR_OI + 1),
                         bar(BAR_OF), bar(BAR_OF + 1), bar(BAR_IE), bar(BAR_IE + 1)};
-    epilogue_loop<CAUSAL>(a, misc, bars, reinterpret_cast<const float*>(smem + SM_INV), n_items, ring,
+    epilogue_loop<CAUSAL, CHUNK>(a, misc, bars, reinterpret_cast<const float*>(smem + SM_INV), n_items, ring,
                           warp, lane);
   }
 
@@ -821,7 +897,7 @@ bool make_btHd_map(CUtensorMap* m, const void* ptr, int B, int T, int H) {
   return encode(m, ptr, 4, dims, strides, box);
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool CHUNK = false>
 int launch_tiles(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                  const TileArgs& a, long n_items, cudaStream_t stream) {
   if (n_items <= 0) return PKV_OK;
@@ -830,13 +906,14 @@ int launch_tiles(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 32 && !(configured_mask & (1 << dev))) {
-    if (check_launch(cudaFuncSetAttribute(attn_tile_kernel<CAUSAL>,
+    if (check_launch(cudaFuncSetAttribute(attn_tile_kernel<CAUSAL, CHUNK>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) != PKV_OK)
       return PKV_ERR_LAUNCH;
     configured_mask |= (1 << dev);
   }
   // One CTA per item: the CTAs that run first take over the rest (work distribution).
-  attn_tile_kernel<CAUSAL><<<(unsigned)n_items, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, a, (int)n_items);
+  attn_tile_kernel<CAUSAL, CHUNK><<<(unsigned)n_items, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, a,
+                                                                                  (int)n_items);
   return check_launch(cudaGetLastError());
 }
 
@@ -914,6 +991,52 @@ int launch_cascade_prefix(const CascadeArgs& c, cudaStream_t stream) {
   if (a.n_chunks != c.prefix_chunks) return PKV_ERR_INVALID_ARG;  // planner guarantees equality
   const long grid = (long)a.n_chunks * c.n_kv_heads * a.n_row_pairs;
   return launch_tiles<false>(mq, mk, mv, a, grid, stream);
+}
+
+// Chunked prefill over the paged cache: the non-causal tile kernel's third mode. A query
+// tile is 128/G new tokens x the G query heads of one KV head (as in the prefix mode), K/V
+// are gathered page by page through each sequence's own block table, and row r of a tile
+// sees the keys up to its own position prefix_len + token.
+int launch_prefill_chunk(const ChunkArgs& c, cudaStream_t stream) {
+  if (c.head_dim != HD || c.page_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int G = c.n_qo_heads / c.n_kv_heads;
+  if (BM % G) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  {
+    // q [B, C, Hq, D] as (D, Hq, C, B): one box = G heads x 128/G tokens = 128 rows of 64
+    cuuint64_t dims[4] = {(cuuint64_t)HD, (cuuint64_t)c.n_qo_heads, (cuuint64_t)c.chunk_len,
+                          (cuuint64_t)c.batch};
+    cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)c.n_qo_heads * HD * 2,
+                             (cuuint64_t)c.chunk_len * c.n_qo_heads * HD * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(BM / G), 1};
+    if (!encode(&mq, c.q, 4, dims, strides, box)) return check_launch(cudaErrorInvalidValue);
+  }
+  {
+    // pools [pages, Hkv, 16, D] as rows of D: one box = one (page, head) tile, 16 rows x 64
+    const cuuint64_t rows = (cuuint64_t)c.num_pages * c.n_kv_heads * 16;
+    cuuint64_t dims[2] = {(cuuint64_t)HD, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)HD * 2};
+    cuuint32_t box[2] = {64, 16};
+    if (!encode(&mk, c.k_pages, 2, dims, strides, box) || !encode(&mv, c.v_pages, 2, dims, strides, box))
+      return check_launch(cudaErrorInvalidValue);
+  }
+  TileArgs a{};
+  a.out = c.out;
+  a.lse = c.lse;
+  a.err_flag = c.err_flag;
+  a.scale = c.scale;
+  a.batch = c.batch;
+  a.n_qo_heads = c.n_qo_heads;
+  a.n_kv_heads = c.n_kv_heads;
+  a.num_pages = c.num_pages;
+  a.block_table = c.block_table;
+  a.prefix_lens = c.prefix_lens;
+  a.chunk_len = c.chunk_len;
+  a.max_blocks = c.max_blocks;
+  const long tpt = BM / G;
+  const long n_qt = (c.chunk_len + tpt - 1) / tpt;
+  const long grid = (n_qt + 1) / 2 * c.n_kv_heads * c.batch;
+  return launch_tiles<false, true>(mq, mk, mv, a, grid, stream);
 }
 
 }  // namespace pkv
