@@ -145,3 +145,27 @@ def test_fp8_arguments_rejected_before_launch(b):
     # the FP8 workspace query matches the bf16 one (same fp32 partials)
     assert b.decode_workspace_size(4, 64, 32, 8, 128, 16, 8, b.PKV_FP8_E4M3) == \
         b.decode_workspace_size(4, 64, 32, 8, 128, 16, 8, b.PKV_BF16)
+
+
+def test_chunked_prefill_arguments_rejected_before_launch(b):
+    L = b.lib
+    p = ctypes.c_void_p(1 << 20)
+    args = lambda **kw: dict(dict(batch=1, chunk=8, max_blocks=4, pages=16, hq=8, hkv=8, d=128, ps=16,
+                                  dtype=b.PKV_BF16, prefix=p), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return L.attn_prefill_paged_chunk(p, p, p, p, a["prefix"], p, None, a["batch"], a["chunk"],
+                                          a["max_blocks"], a["pages"], a["hq"], a["hkv"], a["d"],
+                                          a["ps"], 0.1, a["dtype"], None, None)
+
+    assert call(batch=0) == b.PKV_OK                      # nothing to do
+    assert call(chunk=0) == b.PKV_OK
+    assert call(prefix=None) == b.PKV_ERR_INVALID_ARG      # no prefix lengths
+    assert call(chunk=65) == b.PKV_ERR_INVALID_ARG         # more new tokens than the table holds
+    assert call(hq=6, hkv=4) == b.PKV_ERR_INVALID_ARG      # heads not a multiple
+    assert call(dtype=7) == b.PKV_ERR_INVALID_ARG
+    assert call(d=64) == b.PKV_ERR_UNSUPPORTED             # only head_dim 128 is built
+    assert call(ps=32, max_blocks=2) == b.PKV_ERR_UNSUPPORTED
+    assert call(hq=12, hkv=4) == b.PKV_ERR_UNSUPPORTED     # a group of 3 does not divide 128 rows
+    assert call(dtype=b.PKV_F32) == b.PKV_ERR_UNSUPPORTED
