@@ -16,14 +16,29 @@ int check_launch(cudaError_t e) {
 }
 
 int device_sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // zero-initialised (static storage); 0 = not looked up yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_acquire);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_release);
   return n;
+}
+
+bool FuncConfigured::ensure(const void* func, int smem_bytes) {
+  int dev = 0;
+  if (check_launch(cudaGetDevice(&dev)) != PKV_OK) return false;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit && (mask.load(std::memory_order_acquire) & bit)) return true;
+  if (check_launch(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) !=
+      PKV_OK)
+    return false;
+  if (bit) mask.fetch_or(bit, std::memory_order_release);
+  return true;
 }
 
 SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requested,

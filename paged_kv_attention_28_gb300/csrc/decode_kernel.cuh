@@ -815,14 +815,8 @@ template <typename T, int D, int P, int G, bool UNIFIED, bool FP8 = false>
 int launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
   using C = DecodeCfg<T, D, P, G, UNIFIED, FP8>;
   auto kern = decode_paged_kernel<T, D, P, G, UNIFIED, FP8>;
-  static int configured_mask = 0;  // one bit per device ordinal < 32
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 32 && !(configured_mask & (1 << dev))) {
-    if (check_launch(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM)) != PKV_OK)
-      return PKV_ERR_LAUNCH;
-    configured_mask |= (1 << dev);
-  }
+  static FuncConfigured configured;
+  if (!configured.ensure(reinterpret_cast<const void*>(kern), C::SMEM)) return PKV_ERR_LAUNCH;
   dim3 grid(a.num_splits, a.n_kv_heads / C::HPC, a.batch);
   kern<<<grid, C::THREADS, C::SMEM, stream>>>(a);
   return check_launch(cudaGetLastError());

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the launch layer and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -44,6 +45,15 @@ struct SplitPlan {
 };
 
 int device_sm_count();
+
+// The dynamic shared-memory limit of one kernel, raised once per device before its first
+// launch there. A device's bit is set only after the attribute call has succeeded, so a
+// thread that sees it set launches on a configured kernel; two threads making a first call
+// at the same time may both set the attribute, which is harmless.
+struct FuncConfigured {
+  std::atomic<uint64_t> mask{0};  // one bit per device ordinal < 64
+  bool ensure(const void* func, int smem_bytes);
+};
 
 // Remembers the most recent failing CUDA call of this host thread (see
 // attn_last_cuda_error_string) and returns PKV_ERR_LAUNCH, or PKV_OK on success.
@@ -119,6 +129,7 @@ struct ChunkArgs {
   float scale;
 };
 int launch_prefill_chunk(const ChunkArgs& a, cudaStream_t stream);
+
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream);
 
 }  // namespace pkv

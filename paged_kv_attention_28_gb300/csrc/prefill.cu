@@ -71,13 +71,16 @@ constexpr int SM_BAR = SM_V + NSV * TILE;
 // item's last PV finished). k_empty and v_empty take one arrival from each MMA issuer.
 constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 15,
               BAR_OD = 19, BAR_DRAIN = 21, BAR_QE = 23, BAR_OF = 25, BAR_Q1 = 27, BAR_ST = 28, BAR_IE = 30,
-              BAR_OI = 32, BAR_NF = 34, BAR_NE = 38, NBAR = 42;
+              BAR_OI = 32, BAR_NF = 34, BAR_NE = 38, BAR_VZ = 42, NBAR = 44;
 // next_full[4] / next_empty[4]: a ring of work-distribution responses (below); next_full
 // completes when a response lands (16 bytes), next_empty takes one arrival from every warp.
 constexpr int NXS = 4;
 // q_full and q_empty exist per query tile: tile t's Q uses BAR_Q / BAR_Q1 and BAR_QE + t.
 // st_full[2]: a tile's softmax has written its rows' 1/l for the epilogue warpgroup;
 // inv_empty[2]: the epilogue has read them, so the next item's softmax may overwrite them.
+// v_zeroed (chunk mode): tile B's issuer has zeroed the V rows past the sequence's end in
+// the last key tile that both tiles read (one phase per such item). NBAR stays even so
+// that the structure after the barriers is 16-byte aligned.
 constexpr int SM_INV = SM_BAR + NBAR * 8;          // float [2 tiles][128 rows]: 1/l per row
 constexpr int SM_MISC = SM_INV + 2 * BM * 4;
 constexpr int SMEM_BYTES = SM_MISC + 128 + 1024;  // + slack to align the base to 1024
@@ -89,11 +92,16 @@ constexpr float kLog2eF = 1.4426950408889634f;
 constexpr float kLn2F = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.0f;  // log2 units
 
+constexpr int NBAD = 8;  // bad-page marks kept for the last NBAD items of a CTA
 struct Misc {
   uint4 next[NXS];  // responses of the work-distribution requests (16-byte aligned)
   uint32_t tmem_base;
   int abort_;
-  int bad_page;
+  // bad_item[k % NBAD] holds the id of this CTA's k-th item if one of its table entries
+  // was out of range. Ids are unique within a launch, so a mark left by item k - NBAD
+  // never matches item k; a producer is never NBAD items ahead of the softmax warps
+  // (each item's request for the next one waits for every warp to finish item k - NXS).
+  int bad_item[NBAD];
 };
 static_assert(sizeof(Misc) <= 128 && SM_MISC % 16 == 0, "Misc layout");
 
@@ -234,11 +242,13 @@ struct Item {
   int hk;        // KV head
   int qrow;      // causal: first query row of A; prefix: first (request, head) row of A
   int b;         // causal: batch
+  int id;        // the item's index in the grid
 };
 
 template <bool CAUSAL, bool CHUNK = false>
 __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
   Item it{};
+  it.id = id;
   const int H = a.n_qo_heads;
   const int G = a.n_qo_heads / a.n_kv_heads;
   if constexpr (CHUNK) {
@@ -442,7 +452,8 @@ __device__ __forceinline__ void softmax_loop(const TileArgs& a, Misc* misc, uint
     // divides O once the item's last PV is done.
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && lane == 0) fail(misc, a.err_flag);
-    if (*reinterpret_cast<volatile int*>(&misc->bad_page)) ok = false;
+    // rows of an item that read an out-of-range table entry become NaN (only that item's)
+    if (*reinterpret_cast<volatile int*>(&misc->bad_item[k % NBAD]) == id) ok = false;
     const float lse_row = ok ? (ms + log2f(l)) * kLn2F : NAN;
     if constexpr (CHUNK) {
       const int G = a.n_qo_heads / a.n_kv_heads;
@@ -577,7 +588,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       mbar_init(bar(i), per_thread ? 128 : (per_issuer ? 2 : (per_warp ? THREADS / 32 : 1)));
     }
     misc->abort_ = 0;
-    misc->bad_page = 0;
+    for (int i = 0; i < NBAD; ++i) misc->bad_item[i] = -1;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -610,6 +621,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const bool v_role = warp == 3;
         uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0;
         bool ok = true;
+        uint32_t k = 0, n_req = 0;  // k: this CTA's item count, the current item's sequence number
         // One 128-key tile of K or V (32 KiB) into its ring.
         auto load_tile = [&](const Item& it, int j, bool is_v) -> bool {
           uint32_t& cnt = is_v ? v_cnt : k_cnt;
@@ -625,8 +637,8 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             __syncwarp();
             return true;
           }
-          mbar_arrive_expect_tx(full, TILE);
           if constexpr (CAUSAL) {
+            mbar_arrive_expect_tx(full, TILE);
             const int k0 = j * BN;
             tma_load_4d(dst, map, 0, it.hk, k0, it.b, full);
             tma_load_4d(dst + SUB, map, 64, it.hk, k0, it.b, full);
@@ -637,15 +649,26 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             // chunk: the sequence's own pages, up to its last new token
             const int n_seq_pages = CHUNK ? (it.A.L0 + a.chunk_len + 15) / 16 : a.n_prefix_pages;
             const int32_t* table = CHUNK ? a.block_table + (size_t)it.b * a.max_blocks : a.prefix_table;
+            int phys[8];
+            bool bad = false;
+#pragma unroll
             for (int pp = 0; pp < 8; ++pp) {
               const int page_idx = (it.kv_first + j) * 8 + pp;
-              int phys = __ldg(table + (page_idx < n_seq_pages ? page_idx : 0));
-              if (phys < 0 || phys >= a.num_pages) {
-                misc->bad_page = 1;
-                set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
-                phys = 0;
+              phys[pp] = __ldg(table + (page_idx < n_seq_pages ? page_idx : 0));
+              if (phys[pp] < 0 || phys[pp] >= a.num_pages) {
+                bad = true;
+                phys[pp] = 0;
               }
-              const int row = (phys * a.n_kv_heads + it.hk) * 16;
+            }
+            // The mark is written before the arrival below, which publishes it with the tile.
+            if (bad) {
+              misc->bad_item[k % NBAD] = it.id;
+              set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
+            }
+            mbar_arrive_expect_tx(full, TILE);
+#pragma unroll
+            for (int pp = 0; pp < 8; ++pp) {
+              const int row = (phys[pp] * a.n_kv_heads + it.hk) * 16;
               tma_load_2d(dst + pp * 2048, map, 0, row, full);
               tma_load_2d(dst + SUB + pp * 2048, map, 64, row, full);
             }
@@ -653,7 +676,6 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           __syncwarp();
           return true;
         };
-        uint32_t k = 0, n_req = 0;
         for (int id = blockIdx.x; ok && id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
           const Item it = make_item<CAUSAL, CHUNK>(a, id);
           // Q_t may be replaced once the previous item's last S_t has read it.
@@ -763,7 +785,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           }
           __syncwarp();
         };
-        uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, g = 0, of_cnt = 0, of_need = 0;
+        uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, g = 0, of_cnt = 0, of_need = 0, vz_cnt = 0;
         bool ok = true;
         uint32_t k = 0;
         for (int id = blockIdx.x; ok && id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
@@ -807,18 +829,32 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if constexpr (CHUNK) {
               // The tile holding the sequence's last key also holds page slots past it,
               // whose contents are not the caller's data (they may not even be finite): zero
-              // those V rows, since a masked key still enters PV as 0 x V. Both issuers may
-              // write the same zeros; each makes its writes visible to the tensor core first.
+              // those V rows, since a masked key still enters PV as 0 x V. One issuer zeroes
+              // them: B's when both tiles read that key tile (B's key range contains A's),
+              // and A waits for it before its product; the writes are made visible to the
+              // tensor core first.
               const int pos_end = it.A.L0 + a.chunk_len;  // keys [0, pos_end) exist
-              if (half == 0 && j == (pos_end - 1) / BN) {
-                unsigned char* vt = smem + SM_V + (vg % NSV) * TILE;
-                for (int row = pos_end - j * BN + (lane >> 3); row < BN; row += 4)
+              const int j_last = (pos_end - 1) / BN;
+              if (half == 0 && j == j_last) {
+                const bool b_reads = it.B.n_tiles > 0 && it.B.n_tiles - 1 == j_last;
+                const bool a_reads = it.A.n_tiles - 1 == j_last;
+                if (t == 1 || !b_reads) {
+                  unsigned char* vt = smem + SM_V + (vg % NSV) * TILE;
+                  for (int row = pos_end - j * BN + (lane >> 3); row < BN; row += 4)
 #pragma unroll
-                  for (int sub = 0; sub < 2; ++sub)
-                    *reinterpret_cast<uint4*>(vt + sub * SUB + row * 128 + (lane & 7) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
-                __syncwarp();
+                    for (int sub = 0; sub < 2; ++sub)
+                      *reinterpret_cast<uint4*>(vt + sub * SUB + row * 128 + (lane & 7) * 16) =
+                          make_uint4(0u, 0u, 0u, 0u);
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  if (t == 1 && a_reads) {
+                    if (elect_one()) mbar_arrive(bar(BAR_VZ));
+                    __syncwarp();
+                  }
+                } else {
+                  if (!warp_wait(bar(BAR_VZ), vz_cnt & 1)) { ok = false; break; }
+                  ++vz_cnt;
+                }
               }
             }
             tc_fence_after();
@@ -866,16 +902,17 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   }
 }
 
+// Resolved once per process (a function-local static is initialised by one thread only).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -902,15 +939,9 @@ int launch_tiles(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap
                  const TileArgs& a, long n_items, cudaStream_t stream) {
   if (n_items <= 0) return PKV_OK;
   if (n_items > 0x7fffffffL) return PKV_ERR_UNSUPPORTED;
-  static int configured_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 32 && !(configured_mask & (1 << dev))) {
-    if (check_launch(cudaFuncSetAttribute(attn_tile_kernel<CAUSAL, CHUNK>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) != PKV_OK)
-      return PKV_ERR_LAUNCH;
-    configured_mask |= (1 << dev);
-  }
+  static FuncConfigured configured;
+  if (!configured.ensure(reinterpret_cast<const void*>(attn_tile_kernel<CAUSAL, CHUNK>), SMEM_BYTES))
+    return PKV_ERR_LAUNCH;
   // One CTA per item: the CTAs that run first take over the rest (work distribution).
   attn_tile_kernel<CAUSAL, CHUNK><<<(unsigned)n_items, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, a,
                                                                                   (int)n_items);
