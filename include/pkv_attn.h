@@ -77,6 +77,7 @@ extern "C" {
  *   decode / cascade : head_dim 64 or 128; page_size 16; group size 1, 2, 4 or 8;
  *                      PKV_F32 or PKV_BF16 (cascade: PKV_BF16, head_dim 128)
  *   prefill          : head_dim 128; PKV_BF16; any seq_len >= 1
+ *   flat GEMM        : PKV_BF16; 1 <= m <= 64; k a multiple of 8
  */
 
 /* Human-readable name of a status code. Static storage; never NULL. */
@@ -121,6 +122,10 @@ size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_he
  *   scale : multiplies q . k before the softmax (1/sqrt(head_dim) for the
  *           textbook form)
  *
+ * The pages read K and V through a block table that maps a sequence's logical
+ * blocks to physical pages ("快速注意力内核与算子融合", Q&A on paged attention), and
+ * split the keys into partial softmax states that are combined at the end
+ * ("【FlashAttention-V4，非官方】FlashDecoding++", section 1, on FlashDecoding).
  * One CTA per (sequence, KV head, split) streams that split's K/V pages through
  * the block table into a shared-memory ring. The query heads of the KV head's
  * GQA group are held in registers. Each CTA keeps a running max and sum (online
@@ -157,7 +162,10 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
  *   (num_splits) or a smaller batch fit.
  * - The first call on a device looks up the scratch array's device address
  *   (cudaGetSymbolAddress) with that device current, and caches it. Make that
- *   first call before any stream capture on that device.
+ *   first call before any stream capture on that device. cudaDeviceReset
+ *   destroys the array with the device's context, and the cached address then
+ *   no longer points at it: a process that resets a device must not call this
+ *   entry point on that device afterwards.
  * - Every call on a device shares the one array. Calls whose kernels overlap on
  *   the GPU (different streams, no ordering between them) race on it and give
  *   wrong results; order them, e.g. on one stream. The array keeps the last
@@ -209,7 +217,14 @@ int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void
  *     err_flag are as for attn_decode_paged, with the workspace size from
  *     attn_decode_workspace_size(..., PKV_FP8_E4M3).
  * The result is the attention of attn_decode_paged over the dequantised values, with
- * the per-tile scales applied to the dot products and to the softmax weights. Pools
+ * the per-tile scales applied to the dot products and to the softmax weights.
+ * Arithmetic: codes become f16 exactly; q is scaled per head by a power of two that
+ * brings its largest magnitude to [2^14, 2^15) and converted to f16 (exact for bf16 q,
+ * whatever its range, except for elements more than 2^24 below the head's largest);
+ * dot products and the weighted sums of V accumulate in fp32. A softmax weight times the
+ * tile's V scale enters the V sum as an f16 value (11-bit significand, normal from 2^-14
+ * to 65504): V scales above 65504 are not supported, and below about 2^-14 such a weight
+ * keeps an absolute precision of 2^-24. Pools
  * must be 16-byte aligned. A CTA takes two adjacent KV heads, so n_kv_heads must be
  * even. Built for head_dim 64 and 128, page_size 16 and GQA groups 1, 2, 4 and 8;
  * other shapes return PKV_ERR_UNSUPPORTED.
@@ -320,6 +335,56 @@ int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
                         int n_qo_heads, int n_kv_heads, int head_dim, int page_size, float scale,
                         int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
                         void* stream);
+
+/*
+ * Flat GEMM of the decode phase: y = x w^T for a few tokens ("【FlashAttention-V4，非官方】
+ * FlashDecoding++", section 4, Flat GEMM Optimization with Double Buffering; the problem is
+ * stated in sections 1 and 2). In decode the projections either side of attention see only
+ * a few tokens at a time, so the GEMM is flat (with one token, a GEMV); the page pads the
+ * token dimension with zeros to 8 instead of the libraries' 64 and overlaps the loads of
+ * the next tile with the products of the current one with two shared-memory buffers.
+ *
+ *   x : bf16 [m][k], the m tokens, row-major
+ *   w : bf16 [n][k], the k x n weight operand passed transposed (each of its n columns
+ *       contiguous, as projection weights are stored)
+ *   y : bf16 [m][n] = x w^T, fp32 accumulation, rounded to nearest even; must not alias
+ *       x or w
+ * Built for dtype PKV_BF16, 1 <= m <= 64, k >= 1 a multiple of 8 (16-byte rows), any n;
+ * x and w 16-byte aligned. m = 0 or n = 0 does nothing. Other shapes return
+ * PKV_ERR_UNSUPPORTED. err_flag (nullable) gets PKV_DEVERR_TIMEOUT if a bounded wait gave
+ * up; the 128 columns of y that CTA group owns are then NaN.
+ *
+ * The weights stream through the tcgen05 tensor cores 128 rows at a time (the product's M
+ * dimension); the tokens are the product's N dimension, padded with zeros to 16, 32 or 64
+ * by the TMA loads (16 is the narrowest product with 128 rows). A ring of shared-memory
+ * stages, fed by TMA, overlaps the loads of the next 64-column slice of K with the
+ * products of the current one (the page's double buffering, with more than two buffers).
+ * K is split over a thread-block cluster of up to 8 CTAs, whose partial tiles are summed
+ * through distributed shared memory: one launch, and no workspace.
+ */
+int attn_flat_gemm(const void* x, const void* w, void* y, int m, int n, int k, int dtype,
+                   int32_t* err_flag, void* stream);
+
+/*
+ * Failure-handling hook for tests (the pages have no counterpart). It lets a test make a
+ * bounded wait inside the decode kernel run out, without faulting or hanging anything:
+ * after attn_debug_decode_stall(page, wait_limit_ns) with page >= 0, every launch of
+ * attn_decode_paged, attn_decode_paged_unified_max, attn_decode_paged_fp8 and
+ * attn_decode_paged_noalloc in this process has the producer warp of each CTA withhold
+ * the copies of the page-th page of its split (and the arrival that would announce them),
+ * and every pipeline wait of those launches gives up after wait_limit_ns nanoseconds
+ * (0 keeps the default of 2 s). The consumer waiting for that page then times out: the
+ * kernel ORs PKV_DEVERR_TIMEOUT into err_flag, waits (within the same limit) for the
+ * copies it did issue, writes the CTA's rows (or split partials) as NaN and returns, so
+ * the context stays usable. attn_debug_decode_stall(-1, 0) turns it off. Not for use
+ * beside production calls: the setting is process-wide. Returns PKV_OK, or
+ * PKV_ERR_INVALID_ARG for page < -1 or a limit above 10 s.
+ */
+int attn_debug_decode_stall(int page, unsigned long long wait_limit_ns);
+
+/* How many CTAs (the cluster size, 1..8) share K for this shape on the current device;
+ * a negative PKV_ERR_* code for shapes attn_flat_gemm rejects. */
+int attn_flat_gemm_num_splits(int m, int n, int k);
 
 #ifdef __cplusplus
 }

@@ -34,6 +34,7 @@ EXPORTS = [
     "attn_decode_paged", "attn_decode_paged_unified_max", "attn_merge_states",
     "attn_prefill_causal", "attn_cascade_workspace_size", "attn_decode_cascade",
     "attn_decode_paged_noalloc", "attn_decode_paged_fp8", "attn_prefill_paged_chunk",
+    "attn_flat_gemm", "attn_flat_gemm_num_splits", "attn_debug_decode_stall",
 ]
 
 
@@ -81,6 +82,12 @@ def _load() -> ctypes.CDLL:
     lib.attn_decode_cascade.restype = i32
     lib.attn_decode_cascade.argtypes = ([vp, vp, vp, vp, i32, vp, vp, vp, vp] + [i32] * 7 +
                                         [f32, i32, vp, sz, vp, vp])
+    lib.attn_flat_gemm.restype = i32
+    lib.attn_flat_gemm.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+    lib.attn_debug_decode_stall.restype = i32
+    lib.attn_debug_decode_stall.argtypes = [i32, ctypes.c_ulonglong]
+    lib.attn_flat_gemm_num_splits.restype = i32
+    lib.attn_flat_gemm_num_splits.argtypes = [i32, i32, i32]
     return lib
 
 
@@ -321,3 +328,32 @@ def decode_cascade(q, k_pages, v_pages, prefix_table, prefix_len, suffix_table, 
                                  _ptr(workspace), wsz, _ptr(err_flag), _stream(stream))
     _check(st, "attn_decode_cascade")
     return out, lse
+
+
+# --------------------------------------------------------------------------- flat GEMM
+
+def flat_gemm_num_splits(m, n, k) -> int:
+    """CTAs that share K (one cluster) per 128-row tile of ``w`` for this shape."""
+    r = lib.attn_flat_gemm_num_splits(int(m), int(n), int(k))
+    if r < 0:
+        raise AttnError(r, "attn_flat_gemm_num_splits")
+    return r
+
+
+def flat_gemm(x, w, out=None, err_flag=None, stream=None):
+    """``y = x w^T`` through ``attn_flat_gemm``: ``x`` ``[m, k]``, ``w`` ``[n, k]``, bf16."""
+    m, k = x.shape
+    n = w.shape[0]
+    _need(x, "x")
+    _need(w, "w", x.dtype, (n, k))
+    if out is None:
+        out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+    _need(out, "out", x.dtype, (m, n))
+    st = lib.attn_flat_gemm(_ptr(x), _ptr(w), _ptr(out), m, n, k, _dt(x), _ptr(err_flag), _stream(stream))
+    _check(st, "attn_flat_gemm")
+    return out
+
+
+def debug_decode_stall(page: int, wait_limit_ns: int = 0) -> None:
+    """Failure-handling hook for tests: ``attn_debug_decode_stall`` (``page = -1`` turns it off)."""
+    _check(lib.attn_debug_decode_stall(int(page), int(wait_limit_ns)), "attn_debug_decode_stall")

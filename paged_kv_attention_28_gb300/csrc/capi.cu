@@ -29,6 +29,17 @@ int device_sm_count() {
   return n;
 }
 
+namespace {
+std::atomic<int> g_stall_page{-1};
+std::atomic<uint64_t> g_stall_limit_ns{0};
+}  // namespace
+
+void decode_stall_settings(int* page, uint64_t* wait_limit_ns) {
+  *page = g_stall_page.load(std::memory_order_relaxed);
+  const uint64_t lim = g_stall_limit_ns.load(std::memory_order_relaxed);
+  if (lim > 0) *wait_limit_ns = lim;
+}
+
 bool FuncConfigured::ensure(const void* func, int smem_bytes) {
   int dev = 0;
   if (check_launch(cudaGetDevice(&dev)) != PKV_OK) return false;
@@ -158,6 +169,7 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   a.unified = unified;
   a.phi = phi;
   a.fallback_count = fallback_count;
+  decode_stall_settings(&a.stall_page, &a.wait_limit_ns);
   a.fp8 = fp8;
   a.k_scale = c.k_scale;
   a.v_scale = c.v_scale;
@@ -373,6 +385,31 @@ int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
   w += align_up(rows * suf.num_splits * head_dim * 4, 256);
   a.suf_lse = reinterpret_cast<float*>(w);
   return launch_cascade(a, static_cast<cudaStream_t>(stream));
+}
+
+int attn_debug_decode_stall(int page, unsigned long long wait_limit_ns) {
+  if (page < -1 || wait_limit_ns > 10000000000ull) return PKV_ERR_INVALID_ARG;
+  g_stall_page.store(page, std::memory_order_relaxed);
+  g_stall_limit_ns.store(page < 0 ? 0 : (uint64_t)wait_limit_ns, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+int attn_flat_gemm_num_splits(int m, int n, int k) {
+  if (m < 1 || n < 1 || k < 1) return PKV_ERR_INVALID_ARG;
+  if (m > kFlatGemmMaxM) return PKV_ERR_UNSUPPORTED;
+  return plan_flat_gemm(m, n, k).splits;
+}
+
+int attn_flat_gemm(const void* x, const void* w, void* y, int m, int n, int k, int dtype,
+                   int32_t* err_flag, void* stream) {
+  if (m < 0 || n < 0 || k < 1) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return PKV_OK;
+  if (!x || !w || !y) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_BF16 || m > kFlatGemmMaxM || k % 8) return PKV_ERR_UNSUPPORTED;
+  FlatGemmArgs a{x, w, y, err_flag, m, n, k};
+  return launch_flat_gemm(a, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

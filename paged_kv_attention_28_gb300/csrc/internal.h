@@ -37,7 +37,15 @@ struct DecodeArgs {
   bool fp8;
   const float* k_scale;  // [num_pages][n_kv_heads]
   const float* v_scale;
+  // Stall injection for the failure-handling test (attn_debug_decode_stall): the producer
+  // of every CTA withholds the copies of page `stall_page` of its split (-1: none), and
+  // every bounded wait gives up after wait_limit_ns.
+  int stall_page = -1;
+  uint64_t wait_limit_ns = 2000000000ull;  // the default limit of every bounded wait
 };
+
+// The stall injection that decode launches pick up (process-wide; off by default).
+void decode_stall_settings(int* page, uint64_t* wait_limit_ns);
 
 struct SplitPlan {
   int num_splits;
@@ -130,6 +138,24 @@ struct ChunkArgs {
 };
 int launch_prefill_chunk(const ChunkArgs& a, cudaStream_t stream);
 
+// Flat GEMM of the decode phase: y[m][n] = sum_k x[m][k] * w[n][k], bf16 in and out.
+struct FlatGemmArgs {
+  const void* x;  // bf16 [m][k]
+  const void* w;  // bf16 [n][k]
+  void* y;        // bf16 [m][n]
+  int32_t* err_flag;
+  int m, n, k;
+};
+struct FlatGemmPlan {
+  int tiles;       // 128-row tiles of w
+  int splits;      // CTAs per tile (a cluster) that share K
+  int kc_per_cta;  // 64-column slices of K per CTA
+  int n_kc;        // 64-column slices of K in all
+};
+constexpr int kFlatGemmMaxM = 64;
+int flat_gemm_padded_m(int m);
+FlatGemmPlan plan_flat_gemm(int m, int n, int k);
+int launch_flat_gemm(const FlatGemmArgs& a, cudaStream_t stream);
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream);
 
 }  // namespace pkv

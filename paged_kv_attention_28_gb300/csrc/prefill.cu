@@ -950,6 +950,8 @@ int launch_tiles(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() { return encode_fn(); }
+
 int launch_prefill(const PrefillArgs& p, cudaStream_t stream) {
   if (p.head_dim != HD) return PKV_ERR_UNSUPPORTED;
   const long n_qt = (p.seq_len + BM - 1) / BM;

@@ -436,6 +436,38 @@ def make_cascade(seed: int, n_requests: int, prefix_len: int, suffix_lens, n_qo_
                        torch.tensor(lens, dtype=torch.int32), float(scale), name=name)
 
 
+@dataclass
+class FlatGemmCase:
+    """The decode-phase flat GEMM: ``x[m, k]`` tokens times the transposed weights ``w[n, k]``."""
+    x: torch.Tensor
+    w: torch.Tensor
+    name: str = ""
+
+    @property
+    def m(self) -> int:
+        return self.x.shape[0]
+
+    @property
+    def n(self) -> int:
+        return self.w.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.x.shape[1]
+
+    def bytes_moved(self) -> int:
+        """Bytes a call must move at least: w and x read once, y written once (bf16)."""
+        return 2 * (self.n * self.k + self.m * self.k + self.m * self.n)
+
+
+def make_flat_gemm(seed: int, m: int, n: int, k: int, name: str = "") -> FlatGemmCase:
+    """bf16 ``x ~ N(0, 1)`` and ``w ~ N(0, 1/k)`` (so ``y`` is about N(0, 1)), both rounded to bf16."""
+    g = _gen(seed)
+    x = _normal(g, (m, k), 1.0, torch.bfloat16)
+    w = _normal(g, (n, k), 1.0 / math.sqrt(k), torch.bfloat16)
+    return FlatGemmCase(x, w, name=name)
+
+
 # --------------------------------------------------------------------------------------
 # The five named workloads (seed 1000 + workload number).
 # --------------------------------------------------------------------------------------
@@ -466,6 +498,13 @@ def long_context_gqa_decode(poison: bool = True) -> PagedDecodeCase:
                              name="long_context_gqa_decode")
 
 
+def long_context_gqa8_decode(poison: bool = True) -> PagedDecodeCase:
+    """The long-context batch with 8 query heads per KV head: 64 query heads over 8 KV heads."""
+    return make_paged_decode(1013, 4, 64, 8, 128, 16, [32768] * 4, num_pages=8192,
+                             max_blocks=2048, dtype="bf16", k_std=2.0, poison=poison,
+                             name="long_context_gqa8_decode")
+
+
 LONG_CONTEXT_SPLITS = 32
 
 
@@ -479,3 +518,17 @@ def cascade_shared_prefix_decode(poison: bool = True) -> CascadeCase:
     return make_cascade(1005, 64, 4096, (128, 1024), 32, 8, 128, page_size=16, num_pages=8192,
                         max_suffix_blocks=64, dtype="bf16", poison=poison,
                         name="cascade_shared_prefix_decode")
+
+
+# The flat GEMMs either side of attention in a Llama-2-7B-shaped decode step (hidden size
+# 4096): the fused QKV projection (n = 3 x 4096) and the output projection (n = 4096),
+# for m decode tokens. Synthetic weights of that shape (no trained weights are used).
+LLAMA7B_HIDDEN = 4096
+
+
+def llama7b_qkv_projection(m: int) -> FlatGemmCase:
+    return make_flat_gemm(1100 + m, m, 3 * LLAMA7B_HIDDEN, LLAMA7B_HIDDEN, name=f"llama7b_qkv_projection_m{m}")
+
+
+def llama7b_o_projection(m: int) -> FlatGemmCase:
+    return make_flat_gemm(1200 + m, m, LLAMA7B_HIDDEN, LLAMA7B_HIDDEN, name=f"llama7b_o_projection_m{m}")

@@ -169,3 +169,34 @@ def test_chunked_prefill_arguments_rejected_before_launch(b):
     assert call(ps=32, max_blocks=2) == b.PKV_ERR_UNSUPPORTED
     assert call(hq=12, hkv=4) == b.PKV_ERR_UNSUPPORTED     # a group of 3 does not divide 128 rows
     assert call(dtype=b.PKV_F32) == b.PKV_ERR_UNSUPPORTED
+
+
+def test_flat_gemm_arguments_rejected_before_launch(b):
+    L = b.lib
+    p = ctypes.c_void_p(1 << 20)
+
+    def call(x=p, w=p, y=p, m=8, n=4096, k=4096, dtype=b.PKV_BF16):
+        return L.attn_flat_gemm(x, w, y, m, n, k, dtype, None, None)
+
+    assert call(m=0) == b.PKV_OK                          # nothing to do
+    assert call(n=0) == b.PKV_OK
+    assert call(m=-1) == b.PKV_ERR_INVALID_ARG
+    assert call(k=0) == b.PKV_ERR_INVALID_ARG
+    assert call(x=None) == b.PKV_ERR_INVALID_ARG
+    assert call(y=None) == b.PKV_ERR_INVALID_ARG
+    assert call(w=ctypes.c_void_p((1 << 20) + 2)) == b.PKV_ERR_INVALID_ARG  # not 16-byte aligned
+    assert call(dtype=9) == b.PKV_ERR_INVALID_ARG
+    assert call(dtype=b.PKV_F32) == b.PKV_ERR_UNSUPPORTED  # bf16 only
+    assert call(m=65) == b.PKV_ERR_UNSUPPORTED             # flat: at most 64 tokens
+    assert call(k=100) == b.PKV_ERR_UNSUPPORTED            # rows must be 16-byte multiples
+
+
+def test_flat_gemm_cluster_planning(b):
+    # the split count is a cluster size: 1..8, never more CTAs than 64-column slices of K
+    for m, n, k in [(1, 4096, 4096), (16, 12288, 4096), (64, 128, 64), (8, 1000, 512), (5, 70000, 64)]:
+        s = b.flat_gemm_num_splits(m, n, k)
+        assert 1 <= s <= 8 and s <= (k + 63) // 64
+    assert b.flat_gemm_num_splits(1, 128, 64) == 1          # one slice of K
+    assert b.flat_gemm_num_splits(16, 4096, 4096) == 8      # 32 tiles: the widest cluster
+    assert b.lib.attn_flat_gemm_num_splits(65, 128, 64) == b.PKV_ERR_UNSUPPORTED
+    assert b.lib.attn_flat_gemm_num_splits(0, 128, 64) == b.PKV_ERR_INVALID_ARG
