@@ -342,7 +342,7 @@ decode_paged_kernel(const DecodeArgs a) {
         const int i = base + k;
         const int s = i % C::NSTAGE;
         const int use = i / C::NSTAGE;
-        if (use > 0 && !warp_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+        if (use > 0 && !warp_wait(bar_empty + 8 * s, (use - 1) & 1, a.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -359,6 +359,9 @@ decode_paged_kernel(const DecodeArgs a) {
           }
           if ((badm >> k) & 1u) {
             mbar_arrive(bar_full + 8 * s);  // completes the phase with no data
+          } else if (i == a.stall_page) {
+            // injected stall: neither copies nor an arrival, so this stage's consumer
+            // waits until its limit runs out
           } else {
             // the CTA's HPC heads' tiles of a page are adjacent in the pool: one copy each
             const size_t off = ((size_t)p * a.n_kv_heads + g0) * C::TILE;
@@ -401,33 +404,65 @@ decode_paged_kernel(const DecodeArgs a) {
   float lsum_own = 0.0f;
 
   if (warp < C::NW) {
-    // q as fp32 pairs prescaled by scale*log2(e); FP8: unscaled f16 pairs, the scale and
-    // the tile's k_scale multiply the finished dot product
+    // q as fp32 pairs prescaled by scale*log2(e); FP8: f16 pairs, the scale and the tile's
+    // k_scale multiply the finished dot product.
     using QP = std::conditional_t<FP8, uint32_t, uint64_t>;
     QP q2[G][DP2];
     const float qscale = a.scale * kLog2e;
     const T* qp = static_cast<const T*>(a.q) + ((size_t)b * a.n_qo_heads + g * G) * D;
+    // FP8: each head's q is scaled by a power of two 2^sh that puts its largest magnitude
+    // in [2^14, 2^15), inside the f16 range, before the conversion to f16; a bf16 value in
+    // f16's normal range converts exactly, and the power of two is exact, so the products
+    // see q unchanged up to the values more than 2^24 below the head's largest. 2^-sh then
+    // multiplies the dot product. (Without it a |q| above 65504 would become infinite.)
+    float q_unscale[G];
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi)
+    for (int gi = 0; gi < G; ++gi) q_unscale[gi] = 1.0f;
+    if constexpr (FP8) {
 #pragma unroll
-      for (int c = 0; c < C::NV; ++c)
+      for (int gi = 0; gi < G; ++gi) {
+        float mx = 0.0f;
 #pragma unroll
-        for (int e = 0; e < C::VEC; e += 2) {
-          const T* src = qp + gi * D + c * C::LPT * C::VEC + j * C::VEC + e;
-          if constexpr (FP8) {
-            const __half2 h = __floats2half2_rn(to_f32<T>(src[0]), to_f32<T>(src[1]));
+        for (int c = 0; c < C::NV; ++c)
+#pragma unroll
+          for (int e = 0; e < C::VEC; ++e)
+            mx = fmaxf(mx, fabsf(to_f32<T>(qp[gi * D + c * C::LPT * C::VEC + j * C::VEC + e])));
+#pragma unroll
+        for (int off = 1; off < C::LPT; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        // exponent of mx (0 for zero and subnormals), then sh = 14 - exponent, kept inside
+        // the normal range of a float scale factor
+        const int ex = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+        int sh = mx > 0.0f ? 14 - ex : 0;
+        sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+        const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+        q_unscale[gi] = __uint_as_float((uint32_t)(127 - sh) << 23);
+#pragma unroll
+        for (int c = 0; c < C::NV; ++c)
+#pragma unroll
+          for (int e = 0; e < C::VEC; e += 2) {
+            const T* src = qp + gi * D + c * C::LPT * C::VEC + j * C::VEC + e;
+            const __half2 h = __floats2half2_rn(to_f32<T>(src[0]) * up, to_f32<T>(src[1]) * up);
             q2[gi][(c * C::VEC + e) / 2] = *reinterpret_cast<const uint32_t*>(&h);
-          } else {
+          }
+      }
+    } else {
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+        for (int c = 0; c < C::NV; ++c)
+#pragma unroll
+          for (int e = 0; e < C::VEC; e += 2) {
+            const T* src = qp + gi * D + c * C::LPT * C::VEC + j * C::VEC + e;
             q2[gi][(c * C::VEC + e) / 2] = pk2(to_f32<T>(src[0]) * qscale, to_f32<T>(src[1]) * qscale);
           }
-        }
+    }
 
     const float beta2 = kUnifiedBeta * kLog2e;
     bool first_chunk = true;
     // a head's WPH warps take its pages in turn; every stage is read by one warp per head
     for (int i = warp % C::WPH; i < n_pages; i += C::WPH) {
       const int s = i % C::NSTAGE;
-      if (!mbar_wait(bar_full + 8 * s, (i / C::NSTAGE) & 1)) {
+      if (!mbar_wait(bar_full + 8 * s, (i / C::NSTAGE) & 1, a.wait_limit_ns)) {
         if (lane == 0) {
           flags->abort_ = 1;
           set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
@@ -464,7 +499,7 @@ decode_paged_kernel(const DecodeArgs a) {
               float d0 = 0.0f, d1 = 0.0f;
 #pragma unroll
               for (int e = 0; e < DP2; ++e) fma_h2_f32(q2[gi][e], k2[e], d0, d1);
-              sc[it][gi] = (d0 + d1) * (qscale * ks);
+              sc[it][gi] = ((d0 + d1) * (qscale * ks)) * q_unscale[gi];
             } else {
               uint64_t d2 = 0ull;
 #pragma unroll
@@ -724,7 +759,7 @@ decode_paged_kernel(const DecodeArgs a) {
       const int issued = flags->issued;
       for (int s = 0; s < C::NSTAGE && s < issued; ++s) {
         const int last_use = (issued - 1 - s) / C::NSTAGE;
-        mbar_wait(bar_full + 8 * s, last_use & 1);
+        mbar_wait(bar_full + 8 * s, last_use & 1, a.wait_limit_ns);
       }
     }
     __syncthreads();

@@ -49,10 +49,21 @@ __device__ __forceinline__ void merge_row_warp(int n, LseF lse_of, OF o_of, T* o
   constexpr float kL2e = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
   float M = -INFINITY;
-  for (int i = lane; i < n; i += 32) M = fmaxf(M, lse_of(i));
+  bool bad = false;  // a NaN partial (a failed split); fmaxf alone would skip it
+  for (int i = lane; i < n; i += 32) {
+    const float x = lse_of(i);
+    bad |= x != x;
+    M = fmaxf(M, x);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   T* o_row = out + lane * DL;
+  if (__any_sync(0xffffffffu, bad)) {
+#pragma unroll
+    for (int e = 0; e < DL; ++e) o_row[e] = merge_cast<T>(NAN);
+    if (lse_out && lane == 0) *lse_out = NAN;
+    return;
+  }
   if (n == 0 || M == -INFINITY) {
 #pragma unroll
     for (int e = 0; e < DL; ++e) o_row[e] = merge_cast<T>(0.0f);

@@ -59,20 +59,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits until the phase with the given parity has completed. Returns false
 // (and the caller reports PKV_DEVERR_TIMEOUT) if that takes longer than
-// kWaitTimeoutNs. It never spins forever.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// limit_ns (kWaitTimeoutNs unless a launch asks for less). It never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if ((i & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 
 // A wait taken by every lane of a warp; the result is the same on all lanes, so
 // .sync.aligned instructions that follow never diverge.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitTimeoutNs) {
+  const bool ok = mbar_wait(bar, parity, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -105,3 +105,18 @@ def test_decode_fp8_rejects_missing_scales(b):
                                  bt.shape[1], c.num_pages, 4, 4, 64, 16, c.scale, 1, None, 0, None,
                                  None)
     assert st == b.PKV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("q_mag", [3e5, 1e-7])
+@pytest.mark.parametrize("G", [1, 4])
+def test_fp8_query_far_outside_f16_range(b, q_mag, G):
+    """The kernel takes q through f16 after scaling each head by a power of two: queries
+    whose magnitudes lie far above f16's largest value (65504) or below its smallest
+    normal give the same attention as the oracle's. The softmax scale shrinks or grows by
+    the same factor, so the logits keep the workload's spread."""
+    c = workloads.make_paged_decode_fp8(120 + G, 3, 4 * G, 4, 128, 16, [300, 77, 512], q_std=q_mag,
+                                        scale=1.0 / (q_mag * 128 ** 0.5))
+    assert float(c.q.float().abs().max()) > 65504 or float(c.q.float().abs().max()) < 6.1e-5
+    got = run(b, c, 2)
+    assert got[2] == 0
+    check(got, ref(c), f"fp8 q magnitude {q_mag} G={G}")

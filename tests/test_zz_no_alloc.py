@@ -12,6 +12,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from paged_kv_attention_28_gb300 import workloads
 from tests._compare import assert_close
 
@@ -75,3 +76,39 @@ def test_noalloc_rejects_shapes_beyond_the_scratch_limit(b):
                                        case.kv_lens))
     rc, _, _, _ = _noalloc(b, case, dev, 64)
     assert rc == b.PKV_ERR_WORKSPACE
+
+
+def test_noalloc_call_allocates_no_device_memory_and_matches_the_oracle(b):
+    """With its inputs and outputs already in place, a call leaves the device's free memory
+    unchanged (it allocates nothing, and the scratch array was in place since load time),
+    and its result is the fp64 oracle's."""
+    case = workloads.make_paged_decode(74, 4, 16, 4, 128, 16, [1500, 700, 2048, 33], num_pages=400,
+                                       max_blocks=128, dtype="bf16")
+    q, kp, vp, bt, ln = (t.to("cuda") for t in (case.q, case.k_pages, case.v_pages, case.block_table,
+                                               case.kv_lens))
+    out = torch.empty_like(q)
+    lse = torch.empty((case.batch, case.n_qo_heads), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def call():
+        return b.lib.attn_decode_paged_noalloc(
+            p(q), p(kp), p(vp), p(bt), p(ln), p(out), p(lse), case.batch, case.max_blocks,
+            case.num_pages, case.n_qo_heads, case.n_kv_heads, case.head_dim, case.page_size,
+            case.scale, 8, b.PKV_BF16, p(err), stream)
+
+    assert call() == b.PKV_OK                       # first call on the device: address lookup
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert call() == b.PKV_OK
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    assert int(err.item()) == 0
+    want_o, want_l = oracle.decode_paged(case.q.double().numpy(), case.k_pages.float().numpy(),
+                                         case.v_pages.float().numpy(), case.block_table.numpy(),
+                                         case.kv_lens.numpy(), case.scale)
+    assert_close(out.float().cpu().numpy(), want_o, "bf16", "noalloc out vs oracle")
+    assert_close(lse.cpu().numpy(), want_l, "bf16", "noalloc lse vs oracle")
