@@ -8,14 +8,19 @@ The same JSON line carries the causal prefill figure (bf16, batch 8, T 1024,
 32 heads, d 128) in TFLOP/s of causal FLOPs.
 
 ``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]``.
-With N > 1 it runs under torchrun, one replica per GPU (the path shards by
-sequence with no exchange). Rank 0 prints one JSON line.
+With N > 1 it runs one replica per GPU under torchrun (the path shards by sequence
+with no exchange); started without torchrun, it starts N ranks itself through
+``torch.distributed.run``. Rank 0 prints one JSON line.
+
+The CPU baseline is the fp64 oracle as it stands, timed after the GPU measurements on
+every host core (worker processes, one BLAS thread each) and on one core.
 """
 from __future__ import annotations
 
 import os
 
-# The CPU baseline (the fp64 oracle) runs on one host core: pin BLAS threads before numpy loads.
+# The CPU baseline (the fp64 oracle) runs one BLAS thread per process, the processes spread
+# over the host's cores: pin BLAS threads before numpy loads (spawned workers inherit it).
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -213,23 +218,60 @@ def max_over_ranks(x, world):
 
 # ----------------------------------------------------------------------------- CPU oracle arm
 
-def oracle_decode_rate(case, budget_s=12.0):
-    """Times the fp64 oracle, as it stands, on whole passes over the decode batch until
-    ``budget_s`` has elapsed. Returns (GB/s of algorithmic bytes, passes, seconds)."""
-    import oracle
-    q = case.q.double().numpy()
-    kp = case.k_pages.float().numpy()
-    vp = case.v_pages.float().numpy()
-    bt = case.block_table.numpy()
-    lens = case.kv_lens.numpy()
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        oracle.decode_paged(q, kp, vp, bt, lens, case.scale)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def oracle_decode_rate(case, budget_s, workers):
+    """Times the fp64 oracle, as it stands, on whole passes over the decode batch (every
+    (sequence, KV head) unit) until ``budget_s`` has elapsed, on ``workers`` processes.
+    Returns (GB/s of algorithmic bytes, passes, seconds)."""
+    from oracle import timing
+    r = timing.decode_runner(case.q.double().numpy(), case.k_pages.float().numpy(),
+                             case.v_pages.float().numpy(), case.block_table.numpy(),
+                             case.kv_lens.numpy(), case.scale, workers)
+    try:
+        passes, el = timing.time_passes(r, budget_s)
+    finally:
+        r.close()
     return case.kv_bytes() * passes / el / 1e9, passes, el
+
+
+def oracle_prefill_rate(case, workers):
+    """One timed pass of the fp64 causal-prefill oracle over the whole workload (it builds
+    every 1024 x 1024 score matrix), after an untimed one. Returns (TFLOP/s of causal FLOPs,
+    seconds)."""
+    from oracle import timing
+    r = timing.prefill_runner(case.q.float().numpy(), case.k.float().numpy(), case.v.float().numpy(),
+                              case.scale, workers)
+    try:
+        _, el = timing.time_passes(r, 0.0)
+    finally:
+        r.close()
+    return case.causal_flops() / el / 1e12, el
+
+
+def cpu_baselines(case, budget_s=8.0):
+    """The decode oracle on every host core and on one core."""
+    cores = host_cores()
+    all_rate = oracle_decode_rate(case, budget_s, cores)
+    one_rate = oracle_decode_rate(case, budget_s, 1)
+    return {"value": all_rate[0], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{all_rate[1]} whole pass(es) of the fp64 oracle over the full decode batch in "
+                      f"{all_rate[2]:.1f} s on {cores} worker processes (one BLAS thread each), after one "
+                      "untimed pass",
+            "value_1core": one_rate[0],
+            "sample_1core": f"{one_rate[1]} pass(es) in {one_rate[2]:.1f} s in one process"}
+
+
+def prefill_cpu_baseline(case):
+    cores = host_cores()
+    tf_all, s_all = oracle_prefill_rate(case, cores)
+    tf_one, s_one = oracle_prefill_rate(case, 1)
+    return {"value": tf_all, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"one whole pass of the fp64 causal-prefill oracle (full 1024 x 1024 scores per "
+                      f"(batch, head), causal FLOPs counted) in {s_all:.2f} s on {cores} worker processes",
+            "seconds": s_all, "value_1core": tf_one, "seconds_1core": s_one}
 
 
 def run_reference(args, rank, world):
@@ -238,14 +280,27 @@ def run_reference(args, rank, world):
         return
     from paged_kv_attention_28_gb300 import workloads
     case = workloads.llama7b_batched_decode(poison=False)
-    for _ in range(args.warmup):
-        pass
-    rates, secs = [], []
-    per_step = max(1.0, 10.0 / max(1, args.steps))
-    for _ in range(args.steps):
-        r, passes, el = oracle_decode_rate(case, budget_s=per_step)
-        rates.append(r)
-        secs.append(el / passes)
+    cores = host_cores()
+    from oracle import timing
+    r = timing.decode_runner(case.q.double().numpy(), case.k_pages.float().numpy(),
+                             case.v_pages.float().numpy(), case.block_table.numpy(),
+                             case.kv_lens.numpy(), case.scale, cores)
+    try:
+        for _ in range(args.warmup):
+            r.one_pass()
+        per_step = max(0.5, 20.0 / max(1, args.steps))
+        rates, secs = [], []
+        for _ in range(args.steps):
+            passes, el = 0, 0.0
+            t0 = time.perf_counter()
+            while passes == 0 or el < per_step:
+                r.one_pass()
+                passes += 1
+                el = time.perf_counter() - t0
+            rates.append(case.kv_bytes() * passes / el / 1e9)
+            secs.append(el / passes)
+    finally:
+        r.close()
     value = statistics.mean(rates)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -253,9 +308,9 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "parallelism": f"replicas{world}"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "whole passes of the fp64 oracle over the full decode batch "
-                                   f"(~{per_step:.0f} s per step)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "whole passes of the fp64 oracle over the full decode batch on "
+                                   f"{cores} worker processes (~{per_step:.1f} s per step)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -277,6 +332,11 @@ def run_ours(args, rank, world, local):
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
 
     stream = torch.cuda.current_stream(dev)
+    if args.only in OTHER_PARTS:
+        res = other_workloads(B, workloads, dev, stream, args.steps, hbm_peak, parts=(args.only,))
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "only": args.only, "also": res}), flush=True)
+        return
     if args.only == "prefill":
         pre = prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src)
         if rank == 0:
@@ -284,9 +344,6 @@ def run_ours(args, rank, world, local):
         return
     builder, workload_desc, req_splits = DECODE_WORKLOADS[args.workload]
     case = getattr(workloads, builder)(poison=False)
-    cpu_rate = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_rate = oracle_decode_rate(case, budget_s=12.0)
 
     # The per-step inputs (q, block table, lengths) and outputs (out, lse) each live in one
     # device buffer, so that the end-to-end loop moves them with one copy each way.
@@ -315,9 +372,14 @@ def run_ours(args, rank, world, local):
         B.decode_paged(q, kp, vp, bt, lens, case.scale, num_splits=req_splits, out=out, lse=lse,
                        workspace=ws, err_flag=err)
 
-    for _ in range(max(3, args.warmup)):
+    # Warm-up steps as the timed ones run them (L2 flush, then the call), so that nothing
+    # happens for the first time inside the timed region; then at least half a second of
+    # calls, so that the GPU is at its clocks.
+    for i in range(max(3, args.warmup)):
+        flush_l2(flush, i)
         step()
     torch.cuda.synchronize()
+    busy_for(step, 0.5)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -440,10 +502,6 @@ def run_ours(args, rank, world, local):
         "gpu_launches": launches_per_step * args.steps,
         "wall_s": wall,
     }
-    if cpu_rate is not None:
-        line["cpu_baseline"] = {"value": cpu_rate[0], "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{cpu_rate[1]} whole pass(es) of the fp64 oracle over the same decode batch in {cpu_rate[2]:.1f} s"}
-
     # ---- causal prefill on the same line (its own roofline against dense bf16)
     pre = None
     if args.only == "all":
@@ -453,8 +511,24 @@ def run_ours(args, rank, world, local):
         line["gpu_launches"] += pre.pop("launches")
     if args.only == "all" and args.workload == "llama7b_batched_decode":
         line["also"] = other_workloads(B, workloads, dev, stream, min(args.steps, 200), hbm_peak)
+
+    # ---- the CPU baseline: the fp64 oracle on the host's cores (rank 0, one GPU only), after
+    # every GPU measurement so that no timed GPU region follows an idle GPU
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baselines(case)
+        if pre is not None:
+            pre["cpu_baseline"] = prefill_cpu_baseline(workloads.causal_prefill_llama7b())
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def busy_for(fn, seconds):
+    """Calls ``fn`` until ``seconds`` of wall time have passed (untimed warm-up)."""
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
 
 
 def packed(specs, device, pin=False):
@@ -486,7 +560,8 @@ def flush_l2(buf, i):
 def time_calls(fn, steps, stream, dev):
     """Mean device time (ms) of ``fn`` over ``steps`` calls, L2 flushed before each call."""
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    for _ in range(3):
+    for i in range(3):
+        flush_l2(flush, i)
         fn()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
@@ -500,8 +575,12 @@ def time_calls(fn, steps, stream, dev):
     return sum(a.elapsed_time(b) for a, b in ev) / steps
 
 
-def other_workloads(B, workloads, dev, stream, steps, hbm_peak):
-    """The remaining workloads, each timed on its own: GB/s of algorithmic K/V bytes."""
+OTHER_PARTS = ("fp8", "gqa", "cascade", "chunk", "flat_gemm", "single")
+
+
+def other_workloads(B, workloads, dev, stream, steps, hbm_peak, parts=OTHER_PARTS):
+    """The remaining workloads, each timed on its own: GB/s of algorithmic K/V bytes (TFLOP/s for
+    the chunked prefill). ``parts`` picks which (all by default; one for a profiler capture)."""
     res = {}
 
     def entry(name, nbytes, ms, extra=None):
@@ -512,109 +591,146 @@ def other_workloads(B, workloads, dev, stream, steps, hbm_peak):
             d.update(extra)
         res[name] = d
 
-    # The Llama-7B batch (same lengths, same page order) over FP8 E4M3 page pools with
-    # per-(page, KV head) scales: half the K/V bytes of the bf16 headline.
-    c = workloads.llama7b_batched_decode_fp8(poison=False)
-    q, kc, vc, ks, vs, bt, ln = (t.to(dev) for t in (c.q, c.k_codes, c.v_codes, c.k_scale,
-                                                     c.v_scale, c.block_table, c.kv_lens))
-    out = torch.empty_like(q)
-    lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
-    S = B.decode_num_splits(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads, c.head_dim,
-                            c.page_size, 0, B.PKV_FP8_E4M3)
-    ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
-                                                   c.head_dim, c.page_size, 0, B.PKV_FP8_E4M3), dev)
-    ms = time_calls(lambda: B.decode_paged_fp8(q, kc, vc, ks, vs, bt, ln, c.scale, out=out, lse=lse,
-                                               workspace=ws), steps, stream, dev)
-    toks = int(c.kv_lens.sum())
-    entry("llama7b_batched_decode_fp8", c.kv_bytes(), ms,
-          {"num_splits": S, "tokens_per_s": toks / (ms / 1e3),
-           "bytes_note": "E4M3 codes of every token's K and V plus the scales of the pages read"})
-    del q, kc, vc, ks, vs, bt, ln, ws
+    if "fp8" in parts:
+        # The Llama-7B batch (same lengths, same page order) over FP8 E4M3 page pools with
+        # per-(page, KV head) scales: half the K/V bytes of the bf16 headline.
+        c = workloads.llama7b_batched_decode_fp8(poison=False)
+        q, kc, vc, ks, vs, bt, ln = (t.to(dev) for t in (c.q, c.k_codes, c.v_codes, c.k_scale,
+                                                         c.v_scale, c.block_table, c.kv_lens))
+        out = torch.empty_like(q)
+        lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
+        S = B.decode_num_splits(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads, c.head_dim,
+                                c.page_size, 0, B.PKV_FP8_E4M3)
+        ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
+                                                       c.head_dim, c.page_size, 0, B.PKV_FP8_E4M3), dev)
+        ms = time_calls(lambda: B.decode_paged_fp8(q, kc, vc, ks, vs, bt, ln, c.scale, out=out, lse=lse,
+                                                   workspace=ws), steps, stream, dev)
+        toks = int(c.kv_lens.sum())
+        entry("llama7b_batched_decode_fp8", c.kv_bytes(), ms,
+              {"num_splits": S, "tokens_per_s": toks / (ms / 1e3),
+               "bytes_note": "E4M3 codes of every token's K and V plus the scales of the pages read"})
+        del q, kc, vc, ks, vs, bt, ln, ws
 
-    c = workloads.long_context_gqa_decode(poison=False)
-    q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
-    out = torch.empty_like(q)
-    lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
-    S = workloads.LONG_CONTEXT_SPLITS
-    ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads,
-                                                   c.n_kv_heads, c.head_dim, 16, S, B.PKV_BF16), dev)
-    ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
-                                           lse=lse, workspace=ws), steps, stream, dev)
-    entry("long_context_gqa_decode", c.kv_bytes(), ms, {"num_splits": S})
-    fb = torch.zeros(1, dtype=torch.int32, device=dev)
-    ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
-                                           lse=lse, workspace=ws, unified_phi=0.0,
-                                           fallback_count=fb), steps, stream, dev)
-    entry("long_context_gqa_decode_unified_max", c.kv_bytes(), ms,
-          {"num_splits": S, "phi": 0.0, "fallbacks_total": int(fb.item())})
-    del q, kp, vp, bt, ln, ws
+    if "gqa" in parts:
+        c = workloads.long_context_gqa_decode(poison=False)
+        q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
+        out = torch.empty_like(q)
+        lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
+        S = workloads.LONG_CONTEXT_SPLITS
+        ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads,
+                                                       c.n_kv_heads, c.head_dim, 16, S, B.PKV_BF16), dev)
+        ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
+                                               lse=lse, workspace=ws), steps, stream, dev)
+        entry("long_context_gqa_decode", c.kv_bytes(), ms, {"num_splits": S})
+        fb = torch.zeros(1, dtype=torch.int32, device=dev)
+        ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
+                                               lse=lse, workspace=ws, unified_phi=0.0,
+                                               fallback_count=fb), steps, stream, dev)
+        entry("long_context_gqa_decode_unified_max", c.kv_bytes(), ms,
+              {"num_splits": S, "phi": 0.0, "fallbacks_total": int(fb.item())})
+        del q, kp, vp, bt, ln, ws
+        # the same lengths and pool with 8 query heads per KV head (64 query heads)
+        c = workloads.long_context_gqa8_decode(poison=False)
+        q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
+        out = torch.empty_like(q)
+        lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
+        ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads,
+                                                       c.n_kv_heads, c.head_dim, 16, S, B.PKV_BF16), dev)
+        ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale, num_splits=S, out=out,
+                                               lse=lse, workspace=ws), steps, stream, dev)
+        entry("long_context_gqa8_decode", c.kv_bytes(), ms, {"num_splits": S, "group": 8})
+        del q, kp, vp, bt, ln, ws
 
-    c = workloads.cascade_shared_prefix_decode(poison=False)
-    q, kp, vp, pt, st, sl = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.prefix_table,
-                                                 c.suffix_table, c.suffix_lens))
-    out = torch.empty_like(q)
-    lse = torch.empty(c.n_requests, c.n_qo_heads, dtype=torch.float32, device=dev)
-    ws = B.alloc_workspace(B.cascade_workspace_size(c.n_requests, c.prefix_len, st.shape[1],
-                                                    c.n_qo_heads, c.n_kv_heads, c.head_dim,
-                                                    c.page_size), dev)
-    ms = time_calls(lambda: B.decode_cascade(q, kp, vp, pt, c.prefix_len, st, sl, c.scale, out=out,
-                                             lse=lse, workspace=ws), steps, stream, dev)
-    entry("cascade_shared_prefix_decode", c.kv_bytes(), ms,
-          {"bytes_note": "shared prefix K/V counted once plus every suffix"})
-    del q, kp, vp, pt, st, sl, ws
+    if "cascade" in parts:
+        c = workloads.cascade_shared_prefix_decode(poison=False)
+        q, kp, vp, pt, st, sl = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.prefix_table,
+                                                     c.suffix_table, c.suffix_lens))
+        out = torch.empty_like(q)
+        lse = torch.empty(c.n_requests, c.n_qo_heads, dtype=torch.float32, device=dev)
+        ws = B.alloc_workspace(B.cascade_workspace_size(c.n_requests, c.prefix_len, st.shape[1],
+                                                        c.n_qo_heads, c.n_kv_heads, c.head_dim,
+                                                        c.page_size), dev)
+        ms = time_calls(lambda: B.decode_cascade(q, kp, vp, pt, c.prefix_len, st, sl, c.scale, out=out,
+                                                 lse=lse, workspace=ws), steps, stream, dev)
+        entry("cascade_shared_prefix_decode", c.kv_bytes(), ms,
+              {"bytes_note": "shared prefix K/V counted once plus every suffix"})
+        del q, kp, vp, pt, st, sl, ws
 
-    # Chunked prefill over the paged cache: 8 sequences of Llama-7B heads, each appending
-    # 1024 tokens to a 3072-token prefix (the new tokens' K/V already in the pages).
-    n_seq, C, L0 = 8, 1024, 3072
-    c = workloads.make_paged_decode(1006, n_seq, 32, 32, 128, 16, [L0 + C] * n_seq, dtype="bf16",
-                                    poison=False)
-    gen = torch.Generator().manual_seed(1007)
-    qc = torch.randn((n_seq, C, 32, 128), generator=gen, dtype=torch.float32).to(torch.bfloat16).to(dev)
-    kp, vp, bt = c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev)
-    pl = torch.full((n_seq,), L0, dtype=torch.int32, device=dev)
-    out = torch.empty_like(qc)
-    lse = torch.empty((n_seq, 32, C), dtype=torch.float32, device=dev)
-    ms = time_calls(lambda: B.prefill_paged_chunk(qc, kp, vp, bt, pl, c.scale, out=out, lse=lse),
-                    steps, stream, dev)
-    flops = 4 * 128 * 32 * n_seq * (C * L0 + C * (C + 1) // 2)
-    tf = flops / (ms / 1e3) / 1e12
-    res["chunked_prefill_paged"] = {
-        "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "flops": flops,
-        "frac_of_measured_bf16": tf / peaks()[1],
-        "workload": f"{n_seq} sequences x {C} new tokens after a {L0}-token prefix, 32/32 heads, d 128, "
-                    "page 16, bf16 (attended pairs only)"}
-    del qc, kp, vp, bt, pl, out, lse
+    if "chunk" in parts:
+        # Chunked prefill over the paged cache: 8 sequences of Llama-7B heads, each appending
+        # 1024 tokens to a 3072-token prefix (the new tokens' K/V already in the pages).
+        n_seq, C, L0 = 8, 1024, 3072
+        c = workloads.make_paged_decode(1006, n_seq, 32, 32, 128, 16, [L0 + C] * n_seq, dtype="bf16",
+                                        poison=False)
+        gen = torch.Generator().manual_seed(1007)
+        qc = torch.randn((n_seq, C, 32, 128), generator=gen, dtype=torch.float32).to(torch.bfloat16).to(dev)
+        kp, vp, bt = c.k_pages.to(dev), c.v_pages.to(dev), c.block_table.to(dev)
+        pl = torch.full((n_seq,), L0, dtype=torch.int32, device=dev)
+        out = torch.empty_like(qc)
+        lse = torch.empty((n_seq, 32, C), dtype=torch.float32, device=dev)
+        ms = time_calls(lambda: B.prefill_paged_chunk(qc, kp, vp, bt, pl, c.scale, out=out, lse=lse),
+                        steps, stream, dev)
+        flops = 4 * 128 * 32 * n_seq * (C * L0 + C * (C + 1) // 2)
+        tf = flops / (ms / 1e3) / 1e12
+        res["chunked_prefill_paged"] = {
+            "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "flops": flops,
+            "frac_of_measured_bf16": tf / peaks()[1],
+            "workload": f"{n_seq} sequences x {C} new tokens after a {L0}-token prefix, 32/32 heads, d 128, "
+                        "page 16, bf16 (attended pairs only)"}
+        del qc, kp, vp, bt, pl, out, lse
 
-    c = workloads.single_seq_decode_f32()
-    q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
-    ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale), steps, stream, dev)
-    entry("single_seq_decode_f32", c.kv_bytes(), ms,
-          {"note": "1 MiB of K/V: launch-latency bound; L2 flushed before each call"})
-    # The same call captured once into a CUDA graph and replayed: the library never
-    # allocates, copies to the host or synchronises, so the decode and its split merge
-    # replay as one graph launch on the current buffers.
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-    ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
-                                                   c.head_dim, c.page_size, 0, B.PKV_F32), dev)
+    if "flat_gemm" in parts:
+        # The flat GEMMs either side of attention in a Llama-2-7B-shaped decode step: the QKV
+        # projection (n 12288) and the O projection (n 4096), k 4096, for 1, 8 and 16 tokens.
+        # Bytes moved: the bf16 weights, tokens and result once each (the weights dominate;
+        # the QKV weights, 100 MB, would fit in the L2, which is flushed before every call).
+        fg = {}
+        for proj, builder in (("qkv", workloads.llama7b_qkv_projection), ("o", workloads.llama7b_o_projection)):
+            for m in (1, 8, 16):
+                c = builder(m)
+                x, w = c.x.to(dev), c.w.to(dev)
+                y = torch.empty((m, c.n), dtype=torch.bfloat16, device=dev)
+                ms = time_calls(lambda: B.flat_gemm(x, w, out=y), steps, stream, dev)
+                gbs = c.bytes_moved() / (ms / 1e3) / 1e9
+                fg[f"{proj}_m{m}"] = {"value": gbs, "unit": "GB/s", "ms_per_call": ms, "bytes": c.bytes_moved(),
+                                      "frac_of_measured_hbm": gbs / hbm_peak, "m": m, "n": c.n, "k": c.k,
+                                      "cluster": B.flat_gemm_num_splits(m, c.n, c.k),
+                                      "tflops": 2 * m * c.n * c.k / (ms / 1e3) / 1e12}
+                del x, w, y
+        res["flat_gemm"] = {"workload": "Llama-2-7B-shaped decode projections, bf16 x[m, 4096] w[n, 4096]^T, "
+                                        "synthetic weights", "cases": fg}
 
-    def call():
-        B.decode_paged(q, kp, vp, bt, ln, c.scale, out=out, lse=lse, workspace=ws)
+    if "single" in parts:
+        c = workloads.single_seq_decode_f32()
+        q, kp, vp, bt, ln = (t.to(dev) for t in (c.q, c.k_pages, c.v_pages, c.block_table, c.kv_lens))
+        ms = time_calls(lambda: B.decode_paged(q, kp, vp, bt, ln, c.scale), steps, stream, dev)
+        entry("single_seq_decode_f32", c.kv_bytes(), ms,
+              {"note": "1 MiB of K/V: launch-latency bound; L2 flushed before each call"})
+        # The same call captured once into a CUDA graph and replayed: the library never
+        # allocates, copies to the host or synchronises, so the decode and its split merge
+        # replay as one graph launch on the current buffers.
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
+                                                       c.head_dim, c.page_size, 0, B.PKV_F32), dev)
 
-    side = torch.cuda.Stream(dev)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        call()
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        call()
-    ms = time_calls(graph.replay, steps, stream, dev)
-    entry("single_seq_decode_f32_graph", c.kv_bytes(), ms,
-          {"note": "the same call replayed from a CUDA graph captured once; L2 flushed before each replay"})
+        def call():
+            B.decode_paged(q, kp, vp, bt, ln, c.scale, out=out, lse=lse, workspace=ws)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        ms = time_calls(graph.replay, steps, stream, dev)
+        entry("single_seq_decode_f32_graph", c.kv_bytes(), ms,
+              {"note": "the same call replayed from a CUDA graph captured once; L2 flushed before each replay"})
+
     return res
-
 
 def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src):
     case = workloads.causal_prefill_llama7b()
@@ -627,9 +743,11 @@ def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, 
         if e.status == B.PKV_ERR_UNSUPPORTED:
             return None
         raise
-    for _ in range(max(3, args.warmup)):
-        B.prefill_causal(q, k, v, case.scale, out=out, lse=lse)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for i in range(max(3, args.warmup)):
+        flush_l2(flush, i)
+        B.prefill_causal(q, k, v, case.scale, out=out, lse=lse)
+    busy_for(lambda: B.prefill_causal(q, k, v, case.scale, out=out, lse=lse), 0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(world)
@@ -654,21 +772,35 @@ def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, 
             "launches": args.steps}
 
 
+def torchrun_command(n, port, script, argv):
+    """The command that runs ``script argv`` as ``n`` ranks on this node (127.0.0.1 rendezvous)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr=127.0.0.1", f"--master-port={port}", script] + list(argv)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--master-port", type=int, default=29531,
+                    help="rendezvous port when bench.py starts its own ranks (--gpus N > 1)")
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "prefill"] + list(OTHER_PARTS), default="all",
                     help="run one part only (for profiler captures)")
     ap.add_argument("--workload", choices=sorted(DECODE_WORKLOADS), default="llama7b_batched_decode",
                     help="decode workload of the timed step (the headline is llama7b_batched_decode)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # Not started by torchrun: start N ranks (one replica per GPU) through it.
+        sys.exit(subprocess.call(torchrun_command(args.gpus, args.master_port, os.path.abspath(__file__),
+                                                  sys.argv[1:])))
     rank, world, local = dist_init()
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {world}")
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -58,3 +58,34 @@ def test_reference_arm_rank_nonzero_does_no_work():
         steps = 1
         warmup = 0
     assert bench.run_reference(A(), 1, 2) is None
+
+
+RANK_SCRIPT = """
+import json, os, sys
+sys.path.insert(0, {root!r})
+import bench
+r, w, local = bench.dist_init()
+bench.barrier(w)
+t = bench.max_over_ranks(1.0 + r, w)
+with open(os.path.join({out!r}, "rank%d.json" % r), "w") as f:
+    json.dump([r, w, local, t], f)
+import torch.distributed as dist
+dist.destroy_process_group()
+"""
+
+
+def test_bench_starts_its_own_ranks(tmp_path):
+    """``bench.py --gpus N`` outside torchrun starts N ranks through torchrun's launcher;
+    the command it builds runs two gloo ranks here that rendezvous on 127.0.0.1."""
+    import subprocess
+    sys.path.insert(0, ROOT)
+    import bench
+    script = tmp_path / "rank.py"
+    script.write_text(RANK_SCRIPT.format(root=ROOT, out=str(tmp_path)))
+    cmd = bench.torchrun_command(2, _free_port(), str(script), [])
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run(cmd, env=env, timeout=180, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    import json
+    got = sorted(json.loads((tmp_path / f"rank{i}.json").read_text()) for i in range(2))
+    assert got == [[0, 2, 0, 2.0], [1, 2, 1, 2.0]]
