@@ -126,12 +126,16 @@ size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_he
  * blocks to physical pages ("快速注意力内核与算子融合", Q&A on paged attention), and
  * split the keys into partial softmax states that are combined at the end
  * ("【FlashAttention-V4，非官方】FlashDecoding++", section 1, on FlashDecoding).
- * One CTA per (sequence, KV head, split) streams that split's K/V pages through
- * the block table into a shared-memory ring. The query heads of the KV head's
- * GQA group are held in registers. Each CTA keeps a running max and sum (online
- * softmax) and writes a partial (O, LSE) state. A merge kernel then combines the
- * partials by log-sum-exp. Sequences whose pages fit in one split are written
- * directly. The workspace (device, >= attn_decode_workspace_size bytes, 256-byte
+ * One unit of work is (sequence, KV head, split): that split's K/V pages are
+ * streamed through the block table into a shared-memory ring, with a running max
+ * and sum (online softmax), and a partial (O, LSE) state is written. A merge kernel
+ * then combines the partials by log-sum-exp. Sequences whose pages fit in one split
+ * are written directly. With 1 or 2 query heads per KV head (and for fp32) the dot
+ * products and sums run on the CUDA cores, one CTA per unit, the group's queries in
+ * registers. For bf16, head_dim 128 and 4 or 8 query heads per KV head they run on
+ * the tcgen05 tensor cores: 128-key tiles (8 pages) against the group's queries,
+ * padded to 16, with fp32 accumulators in tensor memory; CTAs take units from the
+ * grid until none is left. The workspace (device, >= attn_decode_workspace_size bytes, 256-byte
  * aligned) holds the partials; its contents on entry do not matter.
  */
 int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
@@ -371,12 +375,13 @@ int attn_flat_gemm(const void* x, const void* w, void* y, int m, int n, int k, i
  * after attn_debug_decode_stall(page, wait_limit_ns) with page >= 0, every launch of
  * attn_decode_paged, attn_decode_paged_unified_max, attn_decode_paged_fp8 and
  * attn_decode_paged_noalloc in this process has the producer warp of each CTA withhold
- * the copies of the page-th page of its split (and the arrival that would announce them),
- * and every pipeline wait of those launches gives up after wait_limit_ns nanoseconds
- * (0 keeps the default of 2 s). The consumer waiting for that page then times out: the
- * kernel ORs PKV_DEVERR_TIMEOUT into err_flag, waits (within the same limit) for the
- * copies it did issue, writes the CTA's rows (or split partials) as NaN and returns, so
- * the context stays usable. attn_debug_decode_stall(-1, 0) turns it off. Not for use
+ * the copies of the page-th page of its split (on the tensor-core path: the K copies of
+ * the 128-key tile that holds it) and the arrival that would announce them, and every
+ * pipeline wait of those launches gives up after wait_limit_ns nanoseconds (0 keeps the
+ * default of 2 s). The consumer waiting for that page then times out: the kernel ORs
+ * PKV_DEVERR_TIMEOUT into err_flag, waits (within the same limit) for the copies it did
+ * issue, writes the rows (or split partials) of the unit it was working on, and of any
+ * later unit it had taken, as NaN and returns, so the context stays usable. attn_debug_decode_stall(-1, 0) turns it off. Not for use
  * beside production calls: the setting is process-wide. Returns PKV_OK, or
  * PKV_ERR_INVALID_ARG for page < -1 or a limit above 10 s.
  */

@@ -78,13 +78,15 @@ bool decode_supported(int dtype, int head_dim, int page_size, int group) {
 }
 
 int launch_decode_partials(const DecodeArgs& a, cudaStream_t stream) {
+  if (decode_tc_supported(a)) return launch_decode_tc(a, stream);
   return a.unified ? dispatch_decode_unified(a, stream) : dispatch_decode<false>(a, stream);
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  const int rc = a.fp8       ? dispatch_decode_fp8(a, stream)
-                 : a.unified ? dispatch_decode_unified(a, stream)
-                             : dispatch_decode<false>(a, stream);
+  const int rc = a.fp8                    ? dispatch_decode_fp8(a, stream)
+                 : decode_tc_supported(a) ? launch_decode_tc(a, stream)
+                 : a.unified              ? dispatch_decode_unified(a, stream)
+                                          : dispatch_decode<false>(a, stream);
   if (rc != PKV_OK) return rc;
   if (a.num_splits > 1) return launch_merge_splits(a, stream);
   return PKV_OK;

@@ -1,0 +1,692 @@
+// Paged decode for GQA groups of 4 or 8 query heads on the sm_103a tensor cores.
+//
+// With G query heads per KV head, every key and value element of the cache takes part
+// in G dot-product terms and G weighted sums. At HBM speed that is, for G = 8, about
+// 110 TFLOP/s of multiply-adds: more than the fp32 CUDA cores deliver, so on CUDA cores
+// a GQA decode is bound by its arithmetic, not by its bytes. Here both products of the
+// online softmax ("快速注意力内核与算子融合", Q&A on FlashAttention tiling; partial states
+// per split as in "【FlashAttention-V4，非官方】FlashDecoding++", section 1) run on tcgen05,
+// with the keys as the 128-row operand:
+//   S^T [128 keys x 16]  = K_tile [128 keys x 128 dims]  . Q^T [128 dims x 16 heads]
+//   O^T [128 dims x 16] += V_tile^T [128 dims x 128 keys] . P^T [128 keys x 16 heads]
+// The group's heads are the products' N = 16 (rows past G are padding). A tile is 128
+// keys = 8 pages of 16, gathered through the block table ("快速注意力内核与算子融合", Q&A on
+// paged attention) by 2-D TMA boxes of one (page, KV head) half-row block each.
+//
+// Work: a unit is (split, KV head, sequence), as for the CUDA-core decode, and writes the
+// same outputs (the final row, or an fp32 partial state for the split merge). The grid
+// has one CTA per unit and one CTA fits on an SM; a running CTA takes the pending units
+// (work_queue.cuh), so the rings and TMEM stay warm from one unit to the next.
+//
+// Warps (224 threads): warp 0 TMA producer of Q and K tiles (and TMEM owner), warp 1 MMA
+// issuer, warp 2 TMA producer of V tiles, warps 3..6 the softmax and the epilogue: thread
+// t of those 128 owns key t of a tile (TMEM lane t) and, at the end of a unit, head-dim t
+// of O. Warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31.
+// TMEM: S^T double-buffered (columns 0..15 and 16..31), O^T in columns 32..47.
+// Shared memory: K and V rings of 3 tiles (32 KiB each), Q (4 KiB), P^T double-buffered
+// (4 KiB each), a small reduction area, the barriers.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "tcgen05.cuh"
+#include "work_queue.cuh"
+
+namespace pkv {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();  // prefill.cu
+
+namespace {
+
+constexpr int TK = 128;                  // keys per tile
+constexpr int TD = 128;                  // head dim
+constexpr int NQ = 16;                   // N of both products: the group, padded
+constexpr int KVT = TK * TD * 2;         // one K or V tile: 32 KiB
+constexpr int KVH = KVT / 2;             // one 64-column half of it: [128 rows][128 bytes]
+constexpr int NSK = 3, NSV = 3;          // ring stages
+constexpr int QB = NQ * TD * 2;          // Q tile: 4 KiB, two halves of [16 rows][128 bytes]
+constexpr int PB = NQ * TK * 2;          // one P^T buffer: 4 KiB, two 64-key halves
+constexpr int SM_K = 0;
+constexpr int SM_V = SM_K + NSK * KVT;
+constexpr int SM_Q = SM_V + NSV * KVT;   // Q double-buffered by unit
+constexpr int SM_P = SM_Q + 2 * QB;
+constexpr int NRED = 5;                  // reduction buffers: per step (2), final sums, fallback maxima (2)
+constexpr int SM_RED = SM_P + 2 * PB;    // float [NRED][4 warps][NQ]
+constexpr int SM_ST = SM_RED + NRED * 4 * NQ * 4;  // float [2 units][NQ][2]: each head's (max, sum)
+constexpr int SM_BAR = SM_ST + 2 * NQ * 2 * 4;
+// barriers (one per stage or buffer): k_full k_empty v_full v_empty (3 each), q_full q_empty,
+// s_full s_empty, p_full p_empty (2 each), o_done, u_done o_free st_full st_empty (2 each, by
+// unit parity), drain, next_full next_empty (4 each), red (5: a reduction's parts are in)
+constexpr int B_KF = 0, B_KE = 3, B_VF = 6, B_VE = 9, B_QF = 12, B_QE = 14, B_SF = 16, B_SE = 18,
+              B_PF = 20, B_PE = 22, B_OD = 24, B_UD = 25, B_OF = 27, B_STF = 29, B_STE = 31, B_DR = 33,
+              B_NF = 34, B_NE = 38, B_RED = 42, NBAR = 48;
+constexpr int SM_MISC = SM_BAR + NBAR * 8;
+constexpr int SMEM = SM_MISC + 128 + 1024;  // + slack to align the base to 1024
+static_assert(SMEM <= 232448, "shared memory per CTA");
+static_assert(SM_MISC % 16 == 0 && SM_Q % 1024 == 0 && SM_P % 1024 == 0, "layout");
+constexpr int THREADS = 352;
+constexpr int NWARP = THREADS / 32;
+constexpr int TMEM_COLS = 64;
+constexpr int COL_S = 0, COL_O = 32;  // S^T buffers at 0 and 16, O^T buffers at 32 and 48
+constexpr float kL2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kSlack = 8.0f;  // lazy rescale: a head's reference max moves when a tile beats it by 8 (log2)
+constexpr int NBADM = 8;
+constexpr float kUnifiedBetaTc = 60.0f;  // unified-max margin, natural-log units (as in the CUDA-core kernel)
+
+struct Misc {
+  uint4 next[NXS];
+  uint32_t tmem_base;
+  int abort_;
+  int bad_item[NBADM];  // as in the tile kernel: the id of this CTA's k-th unit if it met a bad page
+};
+static_assert(sizeof(Misc) <= 128, "Misc");
+
+// One unit: where its keys are and where its rows go.
+struct Unit {
+  int split, hk, b;
+  int first, n_pages, kv_len;  // the split's first page (index into the sequence's table) and count
+  int n_tiles;                 // 128-key tiles (0: nothing to stream)
+  int kind;                    // 0: stream; 1: write NaN (bad length); 2: write 0 / -inf (empty); 3: nothing
+  bool final_write;            // the sequence has one live split: write out / lse directly
+};
+
+__device__ __forceinline__ Unit make_unit(const DecodeArgs& a, int id) {
+  Unit u{};
+  u.split = id % a.num_splits;
+  const int rest = id / a.num_splits;
+  u.hk = rest % a.n_kv_heads;
+  u.b = rest / a.n_kv_heads;
+  u.kv_len = __ldg(a.kv_lens + u.b);
+  if (u.kv_len < 0 || u.kv_len > a.max_blocks * 16) {
+    u.kind = (u.split == 0 && !a.partial_only) ? 1 : 3;
+    return u;
+  }
+  const int nblk = (u.kv_len + 15) / 16;
+  const int n_live = (nblk + a.pages_per_split - 1) / a.pages_per_split;
+  if (n_live == 0) {
+    u.kind = (u.split == 0 && !a.partial_only) ? 2 : 3;
+    return u;
+  }
+  if (u.split >= n_live) {
+    u.kind = 3;
+    return u;
+  }
+  u.first = u.split * a.pages_per_split;
+  u.n_pages = min(a.pages_per_split, nblk - u.first);
+  u.n_tiles = (u.n_pages + 7) / 8;
+  u.final_write = n_live == 1 && !a.partial_only;
+  return u;
+}
+
+// Keys of tile j that exist (the rest of the tile is masked).
+__device__ __forceinline__ int tile_valid(const Unit& u, int j) {
+  const int pages = min(8, u.n_pages - 8 * j);
+  return min(pages * 16, u.kv_len - (u.first + 8 * j) * 16);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
+}
+
+// Sum (or max) of x over the 128 softmax threads, for G heads: warp shuffles, then the four
+// warps' values through shared memory buffer `sel`, published by an mbarrier (four
+// arrivals; `phase` counts the buffer's uses) whose wait is bounded like every other.
+// Returns false if the wait gave up. A buffer is written again only two uses later, once
+// every warp has passed the use in between, i.e. has read it.
+template <int G, bool MAX>
+__device__ __forceinline__ bool block_reduce(float (&x)[G], float* red, int sel, uint32_t bar, uint32_t phase,
+                                             int wq, int lane, uint64_t lim) {
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[h], off);
+      x[h] = MAX ? fmaxf(x[h], y) : x[h] + y;
+    }
+  }
+  float* r = red + sel * 4 * NQ;
+  if (lane < G) {
+    float v = x[0];
+#pragma unroll
+    for (int h = 1; h < G; ++h) v = (lane == h) ? x[h] : v;
+    r[wq * NQ + lane] = v;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  if (!warp_wait(bar, phase & 1, lim)) return false;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float a0 = r[h], a1 = r[NQ + h], a2 = r[2 * NQ + h], a3 = r[3 * NQ + h];
+    x[h] = MAX ? fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) : (a0 + a1) + (a2 + a3);
+  }
+  return true;
+}
+
+// The bitwise OR of w over the 128 softmax threads (same exchange as block_reduce).
+__device__ __forceinline__ bool block_or(uint32_t& w, float* red, int sel, uint32_t bar, uint32_t phase, int wq,
+                                         int lane, uint64_t lim) {
+  w = __reduce_or_sync(0xffffffffu, w);
+  uint32_t* r = reinterpret_cast<uint32_t*>(red + sel * 4 * NQ);
+  if (lane == 0) r[wq] = w;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  if (!warp_wait(bar, phase & 1, lim)) return false;
+  w = (r[0] | r[1]) | (r[2] | r[3]);
+  return true;
+}
+
+// UNIFIED: FlashDecoding++'s asynchronised softmax with a unified maximum value
+// ("【FlashAttention-V4，非官方】FlashDecoding++", sections 1 and 3). Every head's logits are
+// exponentiated against the preset phi, so a tile needs no maximum at all: one OR over the
+// threads tells whether any logit lies above phi + 60 (natural-log units), or, on a unit's
+// first tile, whether a head lies wholly below phi - 60. Only then is the tile's maximum
+// taken, the reference moved as in the CUDA-core kernel and the event counted.
+template <int G, bool UNIFIED>
+__global__ void __launch_bounds__(THREADS, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                 const __grid_constant__ CUtensorMap mv, const DecodeArgs a, int n_units) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  unsigned char* smem = smem_raw + pad;
+  const uint32_t sb = raw + pad;
+  Misc* misc = reinterpret_cast<Misc*>(smem + SM_MISC);
+  auto bar = [&](int i) { return sb + SM_BAR + 8 * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t lim = a.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBAR; ++i) {
+      int cnt = 1;
+      // one arrival from each of the four softmax (or epilogue) warps
+      if ((i >= B_SE && i < B_SE + 2) || (i >= B_PF && i < B_PF + 2) || (i >= B_OF && i < B_OF + 2) ||
+          (i >= B_STF && i < B_STF + 2) || (i >= B_STE && i < B_STE + 2) || (i >= B_RED && i < B_RED + NRED))
+        cnt = 4;
+      if (i >= B_NE && i < B_NE + NXS) cnt = NWARP;
+      mbar_init(bar(i), cnt);
+    }
+    misc->abort_ = 0;
+    for (int i = 0; i < NBADM; ++i) misc->bad_item[i] = -1;
+    fence_mbar_init();
+  }
+  // P^T rows past the group are never written: keep them zero.
+  for (int i = threadIdx.x; i < 2 * PB / 16; i += THREADS)
+    reinterpret_cast<uint4*>(smem + SM_P)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&misc->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const NextRing ring{smem_u32(&misc->next[0]), bar(B_NF), bar(B_NE)};
+
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 0: each unit's Q (double-buffered, so the next unit's Q arrives while this one
+    // runs) and K tiles; warp 2: V tiles. Each waits only on its own ring.
+    const bool v_role = warp == 2;
+    if (elect_one()) {
+      tma_prefetch_desc(v_role ? &mv : &mk);
+      if (!v_role) tma_prefetch_desc(&mq);
+    }
+    __syncwarp();
+    uint32_t cnt = 0, qi = 0, k = 0, n_req = 0;
+    bool ok = true;
+    for (int id = blockIdx.x; ok && id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
+      const Unit u = make_unit(a, id);
+      if (u.kind == 0 && !v_role) {
+        // Q of the group (rows past the group read other heads' q, or 0 past the last head)
+        const uint32_t qb = qi & 1;
+        if (qi >= 2 && !warp_wait(bar(B_QE + qb), ((qi >> 1) - 1) & 1, lim)) ok = false;
+        if (ok && elect_one()) {
+          mbar_arrive_expect_tx(bar(B_QF + qb), QB);
+          tma_load_3d(sb + SM_Q + qb * QB, &mq, 0, u.hk * G, u.b, bar(B_QF + qb));
+          tma_load_3d(sb + SM_Q + qb * QB + QB / 2, &mq, 64, u.hk * G, u.b, bar(B_QF + qb));
+        }
+        __syncwarp();
+      }
+      if (u.kind == 0) ++qi;
+      const int32_t* trow = a.block_table + (size_t)u.b * a.max_blocks;
+      for (int j = 0; ok && j < u.n_tiles; ++j, ++cnt) {
+        const uint32_t s = cnt % NSK, use = cnt / NSK;
+        const uint32_t full = bar((v_role ? B_VF : B_KF) + s);
+        if (use > 0 && !warp_wait(bar((v_role ? B_VE : B_KE) + s), (use - 1) & 1, lim)) {
+          ok = false;
+          break;
+        }
+        if (__any_sync(0xffffffffu, misc->abort_ != 0)) {
+          ok = false;
+          break;
+        }
+        // lane pp < 8 reads the table entry of the tile's page pp (slots past the split
+        // reload the unit's first page: finite data, masked)
+        const int pages = min(8, u.n_pages - 8 * j);
+        int phys = 0;
+        bool bad = false;
+        if (lane < 8) {
+          phys = __ldg(trow + u.first + (lane < pages ? 8 * j + lane : 0));
+          bad = phys < 0 || phys >= a.num_pages;
+          if (bad) phys = 0;
+        }
+        const bool any_bad = __any_sync(0xffffffffu, bad);
+        if (any_bad && lane == 0) {
+          misc->bad_item[k % NBADM] = id;  // written before the arrival that publishes the tile
+          set_err(a.err_flag, PKV_DEVERR_BAD_PAGE);
+        }
+        const uint32_t dst = sb + (v_role ? SM_V : SM_K) + s * KVT;
+        const CUtensorMap* map = v_role ? &mv : &mk;
+        const bool stall = !v_role && a.stall_page >= 8 * j && a.stall_page < 8 * j + 8;
+        __syncwarp();
+        if (lane == 0 && !stall) mbar_arrive_expect_tx(full, KVT);
+        __syncwarp();
+        if (lane < 8 && !stall) {
+          const int row = (phys * a.n_kv_heads + u.hk) * 16;
+          tma_load_2d(dst + lane * 2048, map, 0, row, full);
+          tma_load_2d(dst + KVH + lane * 2048, map, 64, row, full);
+        }
+        __syncwarp();
+      }
+      if (!v_role && ok) {
+        // ask for the next unit once this one's copies are all issued
+        const uint32_t s = k % NXS, uu = k / NXS;
+        if (uu > 0 && !warp_wait(ring.empty0 + 8 * s, (uu - 1) & 1, lim)) ok = false;
+        if (ok) {
+          if (elect_one()) request_next_cta(ring.slot0 + 16 * s, ring.full0 + 8 * s);
+          __syncwarp();
+          ++n_req;
+        }
+      }
+    }
+    if (!v_role && n_req > k && !warp_wait(ring.full0 + 8 * ((n_req - 1) % NXS), ((n_req - 1) / NXS) & 1, lim) &&
+        lane == 0)
+      set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+    if (!ok && lane == 0) {
+      misc->abort_ = 1;
+      set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+    }
+    // every issued copy lands before the shared memory is released (the consumers normally
+    // waited for them already)
+    bool drained = true;
+    const uint32_t ns = v_role ? NSV : NSK;
+    for (uint32_t s = 0; s < ns && s < cnt; ++s)
+      if (!warp_wait(bar((v_role ? B_VF : B_KF) + s), ((cnt - 1 - s) / ns) & 1, lim)) drained = false;
+    for (uint32_t q = 0; !v_role && q < 2 && q < qi; ++q)
+      if (!warp_wait(bar(B_QF + ((qi - 1 - q) & 1)), ((qi - 1 - q) >> 1) & 1, lim)) drained = false;
+    if (!drained && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t idS = idesc_bf16_f32(TK, NQ, false, false);
+    const uint32_t idPV = idesc_bf16_f32(TD, NQ, true, false);
+    const uint64_t dk0 = smem_desc(sb + SM_K, 16, 1024, kSwizzle128B);
+    const uint64_t dq0 = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B);
+    const uint64_t dv0 = smem_desc(sb + SM_V, KVH, 1024, kSwizzle128B);
+    const uint64_t dp0 = smem_desc(sb + SM_P, 16, 1024, kSwizzle128B);
+    uint32_t k_cnt = 0, v_cnt = 0, g = 0, qi = 0, k = 0;
+    bool ok = true;
+    // PV of global step gp (tile jp of unit qi): O^T[qi & 1] (+)= V^T P^T
+    auto issue_pv = [&](uint32_t gp, int jp) -> bool {
+      if (!warp_wait(bar(B_PF + (gp & 1)), (gp >> 1) & 1, lim)) return false;
+      const uint32_t vg = v_cnt + jp;
+      if (!warp_wait(bar(B_VF + vg % NSV), (vg / NSV) & 1, lim)) return false;
+      // O^T[qi & 1] was last read by the epilogue of unit qi - 2
+      if (jp == 0 && qi >= 2 && !warp_wait(bar(B_OF + (qi & 1)), ((qi >> 1) - 1) & 1, lim)) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dv = dv0 + (uint64_t)((vg % NSV) * KVT >> 4);
+        const uint64_t dp = dp0 + (uint64_t)(((gp & 1) * PB) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < TK / 16; ++kk)
+          mma_bf16_ss(tmem + COL_O + (qi & 1) * NQ, dv + (uint64_t)((kk * 2048) >> 4),
+                      dp + (uint64_t)(((kk / 4) * (PB / 2) + (kk % 4) * 32) >> 4), idPV,
+                      (jp > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(B_OD));
+        mma_commit(bar(B_VE + vg % NSV));
+        mma_commit(bar(B_PE + (gp & 1)));
+      }
+      __syncwarp();
+      return true;
+    };
+    for (int id = blockIdx.x; ok && id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
+      const Unit u = make_unit(a, id);
+      if (u.kind != 0) continue;
+      const uint32_t qb = qi & 1;
+      if (!warp_wait(bar(B_QF + qb), (qi >> 1) & 1, lim)) {
+        ok = false;
+        break;
+      }
+      const uint32_t g0 = g;
+      for (int j = 0; j < u.n_tiles; ++j, ++g) {
+        const uint32_t kg = k_cnt + j;
+        if (!warp_wait(bar(B_KF + kg % NSK), (kg / NSK) & 1, lim)) { ok = false; break; }
+        if (g >= 2 && !warp_wait(bar(B_SE + (g & 1)), ((g >> 1) - 1) & 1, lim)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dk = dk0 + (uint64_t)((kg % NSK) * KVT >> 4);
+          const uint64_t dq = dq0 + (uint64_t)((qb * QB) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < TD / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk / 4) * KVH + (kk % 4) * 32) >> 4);
+            const uint64_t offq = (uint64_t)(((kk / 4) * (QB / 2) + (kk % 4) * 32) >> 4);
+            mma_bf16_ss(tmem + COL_S + (g & 1) * NQ, dk + off, dq + offq, idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(B_SF + (g & 1)));
+          mma_commit(bar(B_KE + kg % NSK));
+          if (j == u.n_tiles - 1) mma_commit(bar(B_QE + qb));  // the unit's last product that reads Q
+        }
+        __syncwarp();
+        if (j >= 1 && !issue_pv(g - 1, j - 1)) { ok = false; break; }
+      }
+      if (!ok) break;
+      if (!issue_pv(g0 + u.n_tiles - 1, u.n_tiles - 1)) { ok = false; break; }
+      if (elect_one()) mma_commit(bar(B_UD + qb));
+      __syncwarp();
+      k_cnt += u.n_tiles;
+      v_cnt += u.n_tiles;
+      ++qi;
+    }
+    if (!ok && lane == 0) {
+      misc->abort_ = 1;
+      set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+    }
+    // every issued product finishes before TMEM is freed
+    if (elect_one()) mma_commit(bar(B_DR));
+    __syncwarp();
+    if (!warp_wait(bar(B_DR), 0, lim) && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+  } else if (warp < 7) {
+    // ------------------------------------------------------------------ softmax
+    const int wq = warp & 3;           // TMEM lane quarter of this warp
+    const int t = wq * 32 + lane;      // key of a tile
+    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    const float c = a.scale * kL2e;
+    float* red = reinterpret_cast<float*>(smem + SM_RED);
+    float* stats = reinterpret_cast<float*>(smem + SM_ST);
+    uint32_t g = 0, v_cnt = 0, qi = 0, k = 0, n_fb = 0;
+    bool ok = true;
+    for (int id = blockIdx.x; id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
+      const Unit u = make_unit(a, id);
+      if (u.kind != 0 || !ok) continue;  // the epilogue warps write the rows of the other units
+      const uint32_t qb = qi & 1;
+      float M[G], lp[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        M[h] = UNIFIED ? a.phi * kL2e : -INFINITY;
+        lp[h] = 0.0f;
+      }
+      for (int j = 0; j < u.n_tiles; ++j, ++g) {
+        const uint32_t bsel = g & 1;
+        if (!warp_wait(bar(B_SF + bsel), (g >> 1) & 1, lim)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sr[NQ];
+        tmem_ld16(tmem + lane_addr + COL_S + bsel * NQ, sr);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (elect_one()) mbar_arrive(bar(B_SE + bsel));
+        __syncwarp();
+        const int valid = tile_valid(u, j);
+        float x[G], mt[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          x[h] = t < valid ? __uint_as_float(sr[h]) * c : -INFINITY;
+          mt[h] = x[h];
+        }
+        bool need = false, raise = false;  // the same on every thread
+        float alpha[G];
+        if constexpr (UNIFIED) {
+          // bit 31: a logit above its reference + beta; bit h (first tile): some key of head
+          // h is not below its reference - beta (masked keys are -inf, never)
+          const float beta2 = kUnifiedBetaTc * kL2e;
+          uint32_t w = 0;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            if (x[h] > M[h] + beta2) w |= 1u << 31;
+            if (j == 0 && x[h] >= M[h] - beta2) w |= 1u << h;
+          }
+          if (!block_or(w, red, bsel, bar(B_RED + bsel), g >> 1, wq, lane, lim)) { ok = false; break; }
+          const uint32_t low_heads = j == 0 ? (~w) & ((1u << G) - 1u) : 0u;
+          if ((w >> 31) || low_heads) {
+            const int sel = 3 + (n_fb & 1);
+            if (!block_reduce<G, true>(mt, red, sel, bar(B_RED + sel), n_fb >> 1, wq, lane, lim)) { ok = false; break; }
+            ++n_fb;
+            int events = 0;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const bool hi = mt[h] > M[h] + beta2;
+              const bool lo = j == 0 && mt[h] < M[h] - beta2;
+              alpha[h] = hi ? ex2(M[h] - mt[h]) : 1.0f;  // nothing is accumulated yet when lo
+              if (hi) raise = true;
+              if (hi || lo) {
+                lp[h] *= alpha[h];
+                M[h] = mt[h];
+                ++events;
+              }
+            }
+            need = raise;
+            if (events && t == 0 && a.fallback_count) atomicAdd(a.fallback_count, events);
+          }
+        } else {
+          if (!block_reduce<G, true>(mt, red, bsel, bar(B_RED + bsel), g >> 1, wq, lane, lim)) { ok = false; break; }
+#pragma unroll
+          for (int h = 0; h < G; ++h) need |= mt[h] > M[h] + kSlack;
+          if (need) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float mn = mt[h] > M[h] + kSlack ? mt[h] : M[h];
+              alpha[h] = ex2(M[h] - mn);  // 0 while M = -inf
+              lp[h] *= alpha[h];
+              M[h] = mn;
+            }
+          }
+        }
+        if (need && j > 0) {
+          // O^T changes only once PV of the previous step is done (this step's S came after
+          // the PV two steps back, so that one is the only product pending)
+          if (!warp_wait(bar(B_OD), (g - 1) & 1, lim)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t o[NQ];
+          tmem_ld16(tmem + lane_addr + COL_O + qb * NQ, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < G; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          tmem_st16(tmem + lane_addr + COL_O + qb * NQ, o);
+          tmem_st_wait();
+        }
+        // P^T for this step, bf16, key t in column t of each head's row (128-byte swizzle)
+        if (g >= 2 && !warp_wait(bar(B_PE + bsel), ((g >> 1) - 1) & 1, lim)) { ok = false; break; }
+        unsigned char* pbuf = smem + SM_P + bsel * PB + (t >> 6) * (PB / 2);
+        const int within = t & 63, chunk = within >> 3;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float p = ex2(x[h] - M[h]);
+          lp[h] += p;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + (h >> 3) * 1024 + (h & 7) * 128 + ((chunk ^ (h & 7)) << 4) +
+                                            (within & 7) * 2) = __float2bfloat16_rn(p);
+        }
+        if (valid < TK) {
+          // masked keys enter PV as 0 x V: the V rows past the sequence (not the caller's
+          // data, maybe not finite) are zeroed once the tile has landed
+          const uint32_t vg = v_cnt + j;
+          if (!warp_wait(bar(B_VF + vg % NSV), (vg / NSV) & 1, lim)) { ok = false; break; }
+          if (t >= valid) {
+            unsigned char* vrow = smem + SM_V + (vg % NSV) * KVT + t * 128;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              reinterpret_cast<uint4*>(vrow)[i] = make_uint4(0u, 0u, 0u, 0u);
+              reinterpret_cast<uint4*>(vrow + KVH)[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (elect_one()) mbar_arrive(bar(B_PF + bsel));
+        __syncwarp();
+      }
+      if (!ok) continue;
+      v_cnt += u.n_tiles;
+      // the unit's statistics for the epilogue warps: each head's reference max and sum
+      if (!block_reduce<G, false>(lp, red, 2, bar(B_RED + 2), qi, wq, lane, lim)) {
+        ok = false;
+        continue;
+      }
+      if (qi >= 2 && !warp_wait(bar(B_STE + qb), ((qi >> 1) - 1) & 1, lim)) {
+        ok = false;
+        continue;
+      }
+      if (t < G) {
+        float mh = M[0], lh = lp[0];
+#pragma unroll
+        for (int h = 1; h < G; ++h) {
+          mh = t == h ? M[h] : mh;
+          lh = t == h ? lp[h] : lh;
+        }
+        stats[(qb * NQ + t) * 2] = mh;
+        stats[(qb * NQ + t) * 2 + 1] = lh;
+      }
+      __syncwarp();
+      if (elect_one()) mbar_arrive(bar(B_STF + qb));
+      __syncwarp();
+      ++qi;
+    }
+    if (!ok && lane == 0) {
+      misc->abort_ = 1;
+      set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    // Thread t holds head dim t of O^T. Per unit: wait for its last PV and its statistics,
+    // read O^T (the buffer is then free for unit + 2), write out / lse or the partial state.
+    const int wq = warp & 3;
+    const int t = wq * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+    const float* stats = reinterpret_cast<const float*>(smem + SM_ST);
+    uint32_t qi = 0, k = 0;
+    bool ok = true;
+    for (int id = blockIdx.x; id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
+      const Unit u = make_unit(a, id);
+      const size_t row0 = (size_t)u.b * a.n_qo_heads + (size_t)u.hk * G;  // the group's first row
+      if (u.kind == 1 || u.kind == 2) {
+        const float o = u.kind == 1 ? NAN : 0.0f, l = u.kind == 1 ? NAN : -INFINITY;
+        if (u.kind == 1 && t == 0) set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+        for (int h = 0; h < G; ++h) out[(row0 + h) * TD + t] = __float2bfloat16_rn(o);
+        if (a.lse && t < G) a.lse[row0 + t] = l;
+        continue;
+      }
+      if (u.kind != 0) continue;
+      const uint32_t qb = qi & 1;
+      ++qi;
+      float o[G], mh[G], lh[G];
+      bool good = false;
+      if (ok) {
+        ok = warp_wait(bar(B_STF + qb), ((qi - 1) >> 1) & 1, lim) && warp_wait(bar(B_UD + qb), ((qi - 1) >> 1) & 1, lim);
+        tc_fence_after();
+        uint32_t r[NQ];
+        tmem_ld16(tmem + lane_addr + COL_O + qb * NQ, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          o[h] = __uint_as_float(r[h]);
+          mh[h] = stats[(qb * NQ + h) * 2];
+          lh[h] = stats[(qb * NQ + h) * 2 + 1];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (elect_one()) {
+          mbar_arrive(bar(B_OF + qb));   // O^T[qb] may take unit qi + 1's products
+          mbar_arrive(bar(B_STE + qb));  // the statistics buffer may take unit qi + 1's
+        }
+        __syncwarp();
+        good = ok && *reinterpret_cast<volatile int*>(&misc->bad_item[k % NBADM]) != id;
+        if (!ok && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float val = good ? o[h] / lh[h] : NAN;
+        const float lse = good ? (mh[h] + log2f(lh[h])) * kLn2 : NAN;
+        const size_t row = row0 + h;
+        if (u.final_write) {
+          static_cast<__nv_bfloat16*>(a.out)[row * TD + t] = __float2bfloat16_rn(val);
+          if (a.lse && t == h) a.lse[row] = lse;
+        } else {
+          a.part_o[(row * a.num_splits + u.split) * TD + t] = val;
+          if (t == h) a.part_lse[row * a.num_splits + u.split] = lse;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                 const cuuint32_t* box) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int G, bool UNIFIED>
+int launch_tc(const DecodeArgs& a, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  {
+    // q [B][Hq][128] as (128, Hq, B): a box is 64 columns of 16 heads of one sequence
+    cuuint64_t dims[3] = {(cuuint64_t)TD, (cuuint64_t)a.n_qo_heads, (cuuint64_t)a.batch};
+    cuuint64_t strides[2] = {(cuuint64_t)TD * 2, (cuuint64_t)a.n_qo_heads * TD * 2};
+    cuuint32_t box[3] = {64, NQ, 1};
+    if (!encode_bf16(&mq, a.q, 3, dims, strides, box)) return check_launch(cudaErrorInvalidValue);
+  }
+  {
+    // pools [pages][Hkv][16][128] as rows of 128: a box is one (page, KV head) block of 16 rows x 64
+    const cuuint64_t rows = (cuuint64_t)a.num_pages * a.n_kv_heads * 16;
+    cuuint64_t dims[2] = {(cuuint64_t)TD, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)TD * 2};
+    cuuint32_t box[2] = {64, 16};
+    if (!encode_bf16(&mk, a.k_pages, 2, dims, strides, box) || !encode_bf16(&mv, a.v_pages, 2, dims, strides, box))
+      return check_launch(cudaErrorInvalidValue);
+  }
+  static FuncConfigured configured;
+  if (!configured.ensure(reinterpret_cast<const void*>(decode_tc_kernel<G, UNIFIED>), SMEM)) return PKV_ERR_LAUNCH;
+  const long n_units = (long)a.num_splits * a.n_kv_heads * a.batch;
+  if (n_units <= 0) return PKV_OK;
+  if (n_units > 0x7fffffffL) return PKV_ERR_UNSUPPORTED;
+  decode_tc_kernel<G, UNIFIED><<<(unsigned)n_units, THREADS, SMEM, stream>>>(mq, mk, mv, a, (int)n_units);
+  return check_launch(cudaGetLastError());
+}
+
+}  // namespace
+
+bool decode_tc_supported(const DecodeArgs& a) {
+  const int G = a.n_qo_heads / a.n_kv_heads;
+  return a.dtype == PKV_BF16 && !a.fp8 && a.head_dim == TD && a.page_size == 16 && (G == 4 || G == 8);
+}
+
+int launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
+  const int G = a.n_qo_heads / a.n_kv_heads;
+  if (G == 4) return a.unified ? launch_tc<4, true>(a, stream) : launch_tc<4, false>(a, stream);
+  if (G == 8) return a.unified ? launch_tc<8, true>(a, stream) : launch_tc<8, false>(a, stream);
+  return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

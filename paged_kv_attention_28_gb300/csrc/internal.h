@@ -77,6 +77,9 @@ int launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // Enqueues only the decode kernel (the caller merges the partial states).
 int launch_decode_partials(const DecodeArgs& a, cudaStream_t stream);
 bool decode_supported(int dtype, int head_dim, int page_size, int group);
+// The tensor-core decode (decode_tc.cu): bf16, head_dim 128, page 16, groups of 4 or 8.
+bool decode_tc_supported(const DecodeArgs& a);
+int launch_decode_tc(const DecodeArgs& a, cudaStream_t stream);
 
 int launch_merge_pair(const float* out_a, const float* lse_a, const float* out_b,
                       const float* lse_b, void* out, float* lse, int n_rows, int head_dim,

@@ -49,6 +49,7 @@
 
 #include "internal.h"
 #include "tcgen05.cuh"
+#include "work_queue.cuh"
 
 namespace pkv {
 namespace {
@@ -72,9 +73,9 @@ constexpr int SM_BAR = SM_V + NSV * TILE;
 constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 15,
               BAR_OD = 19, BAR_DRAIN = 21, BAR_QE = 23, BAR_OF = 25, BAR_Q1 = 27, BAR_ST = 28, BAR_IE = 30,
               BAR_OI = 32, BAR_NF = 34, BAR_NE = 38, BAR_VZ = 42, NBAR = 44;
-// next_full[4] / next_empty[4]: a ring of work-distribution responses (below); next_full
-// completes when a response lands (16 bytes), next_empty takes one arrival from every warp.
-constexpr int NXS = 4;
+// next_full[4] / next_empty[4]: a ring of work-distribution responses (work_queue.cuh);
+// next_full completes when a response lands (16 bytes), next_empty takes one arrival from
+// every warp.
 // q_full and q_empty exist per query tile: tile t's Q uses BAR_Q / BAR_Q1 and BAR_QE + t.
 // st_full[2]: a tile's softmax has written its rows' 1/l for the epilogue warpgroup;
 // inv_empty[2]: the epilogue has read them, so the next item's softmax may overwrite them.
@@ -137,63 +138,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void fail(Misc* misc, int32_t* err) {
   misc->abort_ = 1;
   set_err(err, PKV_DEVERR_TIMEOUT);
-}
-
-// ---------------------------------------------------------------- work distribution
-// The grid has one CTA per item, but only one CTA per SM is resident at a time. A
-// running CTA takes further items by cancelling CTAs of its own grid that have not
-// started yet (Blackwell cluster launch control): the hardware hands out the pending
-// CTAs in launch order, so items go, in index order, to whichever CTA asks first,
-// i.e. to the first one to run short of work. Items are numbered longest first.
-//
-// Item 0 of a CTA is its own blockIdx.x. During item k, warp 0 asks for item k + 1;
-// the response lands in ring slot k % NXS. Every warp reads it when it reaches the
-// end of item k and then arrives on that slot's next_empty; a failed response (no
-// pending CTA left) ends every warp's loop, and no request follows it.
-__device__ __forceinline__ void request_next_cta(uint32_t slot, uint32_t full) {
-  mbar_arrive_expect_tx(full, 16);
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
-          slot),
-      "r"(full)
-      : "memory");
-}
-
-// The index of the CTA that a response cancelled, or -1 if it cancelled none.
-__device__ __forceinline__ int response_cta(uint32_t slot) {
-  int x;
-  asm volatile(
-      "{\n\t.reg .b128 rr;\n\t.reg .pred p;\n\t"
-      "ld.shared.b128 rr, [%1];\n\t"
-      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, rr;\n\t"
-      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, rr;\n\t"
-      "@!p mov.b32 %0, -1;\n\t}"
-      : "=r"(x)
-      : "r"(slot)
-      : "memory");
-  return x;
-}
-
-// Where the ring lives: the responses, next_full[0] and next_empty[0] (consecutive).
-struct NextRing {
-  uint32_t slot0, full0, empty0;
-};
-
-// Item k + 1 of this CTA, read by a whole warp at the end of its item k; n_items if
-// there is none (or if the response never came, which is reported).
-__device__ __forceinline__ int next_item(const NextRing& ring, uint32_t k, int n_items, int32_t* err) {
-  const uint32_t s = k % NXS, u = k / NXS;
-  int id = n_items;
-  if (warp_wait(ring.full0 + 8 * s, u & 1)) {
-    const int x = response_cta(ring.slot0 + 16 * s);
-    if (x >= 0 && x < n_items) id = x;
-  } else if ((threadIdx.x & 31) == 0) {
-    set_err(err, PKV_DEVERR_TIMEOUT);
-  }
-  __syncwarp();
-  if (elect_one()) mbar_arrive(ring.empty0 + 8 * s);
-  __syncwarp();
-  return id;
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
