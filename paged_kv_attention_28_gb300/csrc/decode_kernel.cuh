@@ -78,7 +78,10 @@ struct DecodeCfg {
   // on the Llama-7B batch; 4 stages and four CTAs 6012).
   static constexpr int NSTAGE = (G == 1 && sizeof(T) == 2) ? 4 : 8;  // multiple of NW
   static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int MIN_BLOCKS = G >= 8 ? 2 : G > 1 ? 3 : FP8 ? 6 : sizeof(T) == 2 ? 5 : 3;
+  // G = 8 (fp32, head_dim 64 and FP8: the bf16 head_dim-128 groups of 4 and 8 run on the
+  // tensor cores) asks for no occupancy, and fp32 G = 4 at head_dim 128 for two CTAs per
+  // SM, so that q and the accumulators stay in registers instead of spilling.
+  static constexpr int MIN_BLOCKS = G >= 8 ? 1 : (G >= 4 && sizeof(T) == 4 && D >= 128) ? 2 : G > 1 ? 3 : FP8 ? 6 : sizeof(T) == 2 ? 5 : 3;
   // G >= 4: the row's lanes reduce the G dot products by halving exchanges, after which
   // each lane holds one head's full score (reduce_scatter_heads).
   static constexpr bool SCATTER = G >= 4 && G <= LPT;
@@ -872,10 +875,13 @@ int dispatch_decode(const DecodeArgs& a, cudaStream_t stream) {
     return launch_decode_t<TT, DD, 16, GG, UNIFIED>(a, stream);
 #define PKV_DEC_DT(TT)                                             \
   PKV_DEC_CASE(TT, 64, 1) PKV_DEC_CASE(TT, 64, 2) PKV_DEC_CASE(TT, 64, 4) PKV_DEC_CASE(TT, 64, 8) \
-  PKV_DEC_CASE(TT, 128, 1) PKV_DEC_CASE(TT, 128, 2) PKV_DEC_CASE(TT, 128, 4) PKV_DEC_CASE(TT, 128, 8)
+  PKV_DEC_CASE(TT, 128, 1) PKV_DEC_CASE(TT, 128, 2)
   if (a.page_size != 16) return PKV_ERR_UNSUPPORTED;
+  // bf16 at head_dim 128 with 4 or 8 query heads per KV head runs on the tensor cores
+  // (decode_tc.cu) and never reaches this dispatch
   if (a.dtype == PKV_F32) {
     PKV_DEC_DT(float)
+    PKV_DEC_CASE(float, 128, 4) PKV_DEC_CASE(float, 128, 8)
   } else if (a.dtype == PKV_BF16) {
     PKV_DEC_DT(__nv_bfloat16)
   }

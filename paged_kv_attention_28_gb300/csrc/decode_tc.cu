@@ -258,8 +258,23 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         __syncwarp();
       }
       if (u.kind == 0) ++qi;
-      const int32_t* trow = a.block_table + (size_t)u.b * a.max_blocks;
+      if (!v_role && ok) {
+        // ask for the next unit as soon as this one is known, so that the answer is in by
+        // the time this unit's copies are issued (units can be one tile long)
+        const uint32_t s = k % NXS, uu = k / NXS;
+        if (uu > 0 && !warp_wait(ring.empty0 + 8 * s, (uu - 1) & 1, lim)) ok = false;
+        if (ok) {
+          if (elect_one()) request_next_cta(ring.slot0 + 16 * s, ring.full0 + 8 * s);
+          __syncwarp();
+          ++n_req;
+        }
+      }
+      // The unit's table entries, 32 pages (four tiles) per warp-wide load: lane l holds
+      // page 32 c + l of the split; a tile's page pp comes from lane (8 j + pp) % 32.
+      const int32_t* trow = a.block_table + (size_t)u.b * a.max_blocks + u.first;
+      int ent = 0;
       for (int j = 0; ok && j < u.n_tiles; ++j, ++cnt) {
+        if ((j & 3) == 0) ent = (32 * (j >> 2) + lane < u.n_pages) ? __ldg(trow + 32 * (j >> 2) + lane) : 0;
         const uint32_t s = cnt % NSK, use = cnt / NSK;
         const uint32_t full = bar((v_role ? B_VF : B_KF) + s);
         if (use > 0 && !warp_wait(bar((v_role ? B_VE : B_KE) + s), (use - 1) & 1, lim)) {
@@ -270,13 +285,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           ok = false;
           break;
         }
-        // lane pp < 8 reads the table entry of the tile's page pp (slots past the split
-        // reload the unit's first page: finite data, masked)
+        // lane pp < 8 takes the entry of the tile's page pp (slots past the split reload a
+        // page of the unit: finite data, masked)
         const int pages = min(8, u.n_pages - 8 * j);
-        int phys = 0;
+        // (both shuffles are taken by the whole warp; a shuffle under a lane-dependent
+        // condition with a full mask is undefined)
+        const int own = __shfl_sync(0xffffffffu, ent, (8 * j + (lane & 7)) & 31);
+        const int tile_first = __shfl_sync(0xffffffffu, ent, (8 * j) & 31);
+        int phys = lane < pages ? own : tile_first;
         bool bad = false;
         if (lane < 8) {
-          phys = __ldg(trow + u.first + (lane < pages ? 8 * j + lane : 0));
           bad = phys < 0 || phys >= a.num_pages;
           if (bad) phys = 0;
         }
@@ -297,16 +315,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           tma_load_2d(dst + KVH + lane * 2048, map, 64, row, full);
         }
         __syncwarp();
-      }
-      if (!v_role && ok) {
-        // ask for the next unit once this one's copies are all issued
-        const uint32_t s = k % NXS, uu = k / NXS;
-        if (uu > 0 && !warp_wait(ring.empty0 + 8 * s, (uu - 1) & 1, lim)) ok = false;
-        if (ok) {
-          if (elect_one()) request_next_cta(ring.slot0 + 16 * s, ring.full0 + 8 * s);
-          __syncwarp();
-          ++n_req;
-        }
       }
     }
     if (!v_role && n_req > k && !warp_wait(ring.full0 + 8 * ((n_req - 1) % NXS), ((n_req - 1) / NXS) & 1, lim) &&
