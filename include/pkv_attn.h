@@ -135,8 +135,8 @@ size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_he
  * registers. For bf16, head_dim 128 and 4 or 8 query heads per KV head they run on
  * the tcgen05 tensor cores: 128-key tiles (8 pages) against the group's queries,
  * padded to 16, with fp32 accumulators in tensor memory; CTAs take units from the
- * grid until none is left. The workspace (device, >= attn_decode_workspace_size bytes, 256-byte
- * aligned) holds the partials; its contents on entry do not matter.
+ * grid until none is left. The workspace (device, >= attn_decode_workspace_size bytes,
+ * 256-byte aligned) holds the partials; its contents on entry do not matter.
  */
 int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                       const int32_t* block_table, const int32_t* kv_lens, void* out, float* lse,
@@ -327,10 +327,16 @@ size_t attn_cascade_workspace_size(int n_requests, int prefix_len, int max_suffi
  * The result equals attn_decode_paged over the concatenated sequences, up to
  * rounding.
  *
- * The prefix product runs on a side stream of the library's (one per device,
- * created with two events on first use and kept for the life of the process),
- * forked from and joined back into `stream` with events, so that it overlaps the
- * suffix decode; the call still completes in `stream` order and may be captured.
+ * With 4 or 8 query heads per KV head (bf16, head_dim 128) the suffix runs on the
+ * tensor-core decode, one unit per (request, KV head), launched on `stream` right after
+ * the prefix product so that it starts while the prefix product finishes (programmatic
+ * dependent launch); each unit waits for the prefix grid only before it merges the
+ * prefix's partial states with its own and writes the request's rows. Other groups run
+ * the prefix product on a side stream of the library's (one per device, created with two
+ * events on first use and kept for the life of the process), forked from and joined back
+ * into `stream` with events, so that it overlaps the CUDA-core suffix decode, and a merge
+ * kernel combines the states. Either way the call completes in `stream` order and may be
+ * captured.
  */
 int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
                         const int32_t* prefix_block_table, int prefix_len,

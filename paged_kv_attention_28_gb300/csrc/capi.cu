@@ -87,11 +87,14 @@ SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requ
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-static size_t decode_ws_bytes(int batch, int n_qo_heads, int head_dim, int S) {
+// Split partials: O [rows][S][D], LSE [rows][S].
+static size_t decode_ws_bytes(int batch, int n_qo_heads, int n_kv_heads, int head_dim, int S) {
+  (void)n_kv_heads;
   if (S <= 1) return 0;
   const size_t rows = (size_t)batch * n_qo_heads;
   return align_up(rows * S * head_dim * sizeof(float), 256) + align_up(rows * S * sizeof(float), 256);
 }
+
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -133,7 +136,7 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, fp8 ? c.n_kv_heads / 2 : c.n_kv_heads,
                                             c.num_splits,
                                             decode_ctas_per_sm(fp8 ? PKV_FP8_E4M3 : c.dtype, c.head_dim, G));
-  const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.head_dim, plan.num_splits);
+  const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.n_kv_heads, c.head_dim, plan.num_splits);
   if (need > 0 && (!c.workspace || c.workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(c.workspace) & 255u) != 0))
     return PKV_ERR_WORKSPACE;
@@ -150,9 +153,10 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   a.lse = c.lse;
   const size_t rows = (size_t)c.batch * c.n_qo_heads;
   if (need > 0) {
-    a.part_o = static_cast<float*>(c.workspace);
-    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(c.workspace) +
-                                          align_up(rows * plan.num_splits * c.head_dim * sizeof(float), 256));
+    char* w = static_cast<char*>(c.workspace);
+    a.part_o = reinterpret_cast<float*>(w);
+    w += align_up(rows * plan.num_splits * c.head_dim * sizeof(float), 256);
+    a.part_lse = reinterpret_cast<float*>(w);
   }
   a.err_flag = c.err_flag;
   a.batch = c.batch;
@@ -218,7 +222,7 @@ size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_he
   const int S = attn_decode_num_splits(batch, max_blocks_per_seq, n_qo_heads, n_kv_heads,
                                        head_dim, page_size, num_splits, dtype);
   if (S < 0) return (size_t)-1;
-  return decode_ws_bytes(batch, n_qo_heads, head_dim, S);
+  return decode_ws_bytes(batch, n_qo_heads, n_kv_heads, head_dim, S);
 }
 
 int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,

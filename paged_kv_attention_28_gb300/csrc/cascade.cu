@@ -66,9 +66,13 @@ int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_q
   const long row_pairs = ((long)n_requests * G + 255) / 256;
   int sms = device_sm_count();
   if (sms <= 0) sms = 148;
-  // About half the SMs for the prefix, and at least four key tiles per chunk so that
-  // each CTA's query load and partial-state write are amortised.
-  long want = sms / ((long)n_kv_heads * row_pairs);
+  // The CUDA-core suffix path runs the prefix beside the suffix decode with one item per SM
+  // at most. The tensor-core path starts the suffix while the prefix runs, and each suffix
+  // unit merges every prefix chunk itself: about 40 % of the SMs for the prefix there, and
+  // at most 8 chunks. At least two key tiles per chunk either way.
+  const bool tc = cascade_uses_tc(n_qo_heads, n_kv_heads, 128, page_size, PKV_BF16);
+  long want = (tc ? (2 * sms) / 5 : sms) / ((long)n_kv_heads * row_pairs);
+  if (tc && want > 8) want = 8;
   const long max_chunks = (n_tiles + 1) / 2;
   if (want > max_chunks) want = max_chunks;
   if (want < 1) want = 1;
@@ -76,8 +80,21 @@ int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_q
   return (n_tiles + tpc - 1) / tpc;
 }
 
+bool cascade_uses_tc(int n_qo_heads, int n_kv_heads, int head_dim, int page_size, int dtype) {
+  DecodeArgs d{};
+  d.n_qo_heads = n_qo_heads;
+  d.n_kv_heads = n_kv_heads;
+  d.head_dim = head_dim;
+  d.page_size = page_size;
+  d.dtype = dtype;
+  return n_kv_heads > 0 && n_qo_heads % n_kv_heads == 0 && decode_tc_supported(d);
+}
+
 SplitPlan cascade_suffix_plan(int n_requests, int max_suffix_blocks, int n_qo_heads,
                               int n_kv_heads, int head_dim, int dtype) {
+  // Tensor-core suffix: one unit per (request, KV head) over all its pages, which merges
+  // the prefix chunks itself.
+  if (cascade_uses_tc(n_qo_heads, n_kv_heads, head_dim, 16, dtype)) return SplitPlan{1, max_suffix_blocks};
   SplitPlan p = plan_decode_splits(n_requests, max_suffix_blocks, n_kv_heads, 0,
                                    decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads));
   // Suffix lengths vary widely from request to request, and the merge that follows
@@ -120,6 +137,42 @@ int side_stream_for_current_device(SideStream** out) {
 }  // namespace
 
 int launch_cascade(const CascadeArgs& a, cudaStream_t stream) {
+  if (cascade_uses_tc(a.n_qo_heads, a.n_kv_heads, a.head_dim, a.page_size, a.dtype) && a.suffix_splits == 1) {
+    // 1) the shared prefix, once per KV head for all requests (tensor cores), on the stream;
+    // 2) each request's suffix on the tensor-core decode, launched to overlap the prefix
+    //    kernel's end; each unit merges the prefix chunks with its own state and writes the
+    //    final rows (no side stream, no merge launch).
+    if (a.prefix_len > 0) {
+      const int rc = launch_cascade_prefix(a, stream);
+      if (rc != PKV_OK) return rc;
+    }
+    DecodeArgs d{};
+    d.q = a.q;
+    d.k_pages = a.k_pages;
+    d.v_pages = a.v_pages;
+    d.block_table = a.suffix_table;
+    d.kv_lens = a.suffix_lens;
+    d.out = a.out;
+    d.lse = a.lse;
+    d.err_flag = a.err_flag;
+    d.batch = a.n_requests;
+    d.max_blocks = a.max_suffix_blocks;
+    d.num_pages = a.num_pages;
+    d.n_qo_heads = a.n_qo_heads;
+    d.n_kv_heads = a.n_kv_heads;
+    d.head_dim = a.head_dim;
+    d.page_size = a.page_size;
+    d.num_splits = 1;
+    d.pages_per_split = a.max_suffix_blocks;
+    d.scale = a.scale;
+    d.dtype = a.dtype;
+    if (a.prefix_len > 0) {
+      d.pre_o = a.pre_o;
+      d.pre_lse = a.pre_lse;
+      d.pre_n = a.prefix_chunks;
+    }
+    return launch_decode_tc(d, stream);
+  }
   // 1) the shared prefix, once per KV head for all requests (tensor cores), on the side
   //    stream: it uses few CTAs, and the suffix decode below fills the other SMs.
   SideStream* side = nullptr;

@@ -18,13 +18,18 @@
 // has one CTA per unit and one CTA fits on an SM; a running CTA takes the pending units
 // (work_queue.cuh), so the rings and TMEM stay warm from one unit to the next.
 //
-// Warps (224 threads): warp 0 TMA producer of Q and K tiles (and TMEM owner), warp 1 MMA
-// issuer, warp 2 TMA producer of V tiles, warps 3..6 the softmax and the epilogue: thread
-// t of those 128 owns key t of a tile (TMEM lane t) and, at the end of a unit, head-dim t
+// With one split per sequence the units' lengths differ as the sequences do; every CTA then
+// ranks the sequences by length (a counting sort over 128-key tiles) and hands out the
+// longest first, so that the last units to start are short ones.
+//
+// Warps (352 threads): warp 0 TMA producer of Q and K tiles (and TMEM owner), warp 1 MMA
+// issuer, warp 2 TMA producer of V tiles, warps 3..6 the softmax: thread t of those 128
+// owns key t of a tile (TMEM lane t); warps 7..10 the epilogue: thread t owns head-dim t
 // of O. Warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31.
-// TMEM: S^T double-buffered (columns 0..15 and 16..31), O^T in columns 32..47.
-// Shared memory: K and V rings of 3 tiles (32 KiB each), Q (4 KiB), P^T double-buffered
-// (4 KiB each), a small reduction area, the barriers.
+// TMEM: S^T double-buffered (columns 0..15 and 16..31), O^T double-buffered by unit
+// (columns 32..47 and 48..63).
+// Shared memory: K and V rings of 3 tiles (32 KiB each), Q and P^T double-buffered (4 KiB
+// each), a small reduction area, the barriers, the sequence order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -64,7 +69,13 @@ constexpr int B_KF = 0, B_KE = 3, B_VF = 6, B_VE = 9, B_QF = 12, B_QE = 14, B_SF
               B_PF = 20, B_PE = 22, B_OD = 24, B_UD = 25, B_OF = 27, B_STF = 29, B_STE = 31, B_DR = 33,
               B_NF = 34, B_NE = 38, B_RED = 42, NBAR = 48;
 constexpr int SM_MISC = SM_BAR + NBAR * 8;
-constexpr int SMEM = SM_MISC + 128 + 1024;  // + slack to align the base to 1024
+constexpr int LPT_MAX = 2048;            // longest-first order for batches up to this size
+constexpr int LPT_BUCKETS = 64;          // by 128-key tiles; 63 or more share the first bucket
+constexpr int SM_HIST = SM_MISC + 128;   // int [LPT_BUCKETS]
+constexpr int SM_ORD = SM_HIST + LPT_BUCKETS * 4;  // uint16 [LPT_MAX]: sequences, longest first
+constexpr int SM_BK = SM_ORD + LPT_MAX * 2;        // uint8 [LPT_MAX]: each sequence's bucket
+constexpr int SMEM = SM_BK + LPT_MAX + 1024;       // + slack to align the base to 1024
+static_assert(LPT_BUCKETS == 64 && LPT_MAX <= 65536, "the order's scan and index type");
 static_assert(SMEM <= 232448, "shared memory per CTA");
 static_assert(SM_MISC % 16 == 0 && SM_Q % 1024 == 0 && SM_P % 1024 == 0, "layout");
 constexpr int THREADS = 352;
@@ -90,16 +101,27 @@ struct Unit {
   int split, hk, b;
   int first, n_pages, kv_len;  // the split's first page (index into the sequence's table) and count
   int n_tiles;                 // 128-key tiles (0: nothing to stream)
+  int n_live;                  // splits of the sequence that hold keys
   int kind;                    // 0: stream; 1: write NaN (bad length); 2: write 0 / -inf (empty); 3: nothing
   bool final_write;            // the sequence has one live split: write out / lse directly
 };
 
-__device__ __forceinline__ Unit make_unit(const DecodeArgs& a, int id) {
+// A sequence's place in the longest-first order: its 128-key tiles, most first; a length
+// the table cannot hold makes a unit that only writes NaN, so it goes last.
+__device__ __forceinline__ int lpt_bucket(const DecodeArgs& a, int b) {
+  const int len = __ldg(a.kv_lens + b);
+  if (len < 0 || len > a.max_blocks * 16) return LPT_BUCKETS - 1;
+  return LPT_BUCKETS - 1 - min((len + TK - 1) / TK, LPT_BUCKETS - 1);
+}
+
+// `ord`: the sequences in the order their units are handed out, or null for batch order.
+__device__ __forceinline__ Unit make_unit(const DecodeArgs& a, int id, const uint16_t* ord) {
   Unit u{};
   u.split = id % a.num_splits;
   const int rest = id / a.num_splits;
   u.hk = rest % a.n_kv_heads;
   u.b = rest / a.n_kv_heads;
+  if (ord) u.b = ord[u.b];
   u.kv_len = __ldg(a.kv_lens + u.b);
   if (u.kv_len < 0 || u.kv_len > a.max_blocks * 16) {
     u.kind = (u.split == 0 && !a.partial_only) ? 1 : 3;
@@ -115,6 +137,7 @@ __device__ __forceinline__ Unit make_unit(const DecodeArgs& a, int id) {
     u.kind = 3;
     return u;
   }
+  u.n_live = n_live;
   u.first = u.split * a.pages_per_split;
   u.n_pages = min(a.pages_per_split, nblk - u.first);
   u.n_tiles = (u.n_pages + 7) / 8;
@@ -184,13 +207,82 @@ __device__ __forceinline__ bool block_or(uint32_t& w, float* red, int sel, uint3
   return true;
 }
 
+// Cascade: head dim t of the G rows of a request's KV head group (rows row0 .. row0 + G - 1):
+// the shared prefix's chunk states are merged by log-sum-exp with the suffix's own (val,
+// lse in natural-log units; lse = -inf for no suffix keys), as the split merge does, and a
+// NaN state makes the row NaN. The chunks' values of all G rows are loaded 32 / G chunks at a
+// time, every load of a batch in flight before any is used.
+template <int G>
+__device__ __forceinline__ void cascade_merge_group(const DecodeArgs& a, size_t row0, int t, float (&val)[G],
+                                                    float (&lse)[G]) {
+  constexpr int CB = 32 / G;  // chunks per batch
+  const size_t stride = (size_t)a.batch * a.n_qo_heads;  // rows per chunk
+  float M[G], l[G], acc[G];
+  bool nan[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    nan[h] = lse[h] != lse[h];
+    M[h] = lse[h];
+    l[h] = lse[h] == -INFINITY ? 0.0f : 1.0f;
+    acc[h] = lse[h] == -INFINITY ? 0.0f : val[h];
+  }
+  for (int c0 = 0; c0 < a.pre_n; c0 += CB) {
+    float L[G][CB], O[G][CB];
+#pragma unroll
+    for (int i = 0; i < CB; ++i)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const int c = c0 + i;
+        const size_t r = (size_t)c * stride + row0 + h;
+        L[h][i] = c < a.pre_n ? __ldcg(a.pre_lse + r) : -INFINITY;
+        O[h][i] = c < a.pre_n ? __ldcg(a.pre_o + r * TD + t) : 0.0f;
+      }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float Mn = M[h];
+#pragma unroll
+      for (int i = 0; i < CB; ++i) {
+        nan[h] |= L[h][i] != L[h][i];
+        Mn = fmaxf(Mn, L[h][i]);
+      }
+      if (Mn == -INFINITY) continue;
+      const float sc = ex2((M[h] - Mn) * kL2e);  // 0 while M = -inf
+      l[h] *= sc;
+      acc[h] *= sc;
+#pragma unroll
+      for (int i = 0; i < CB; ++i) {
+        const float w = ex2((L[h][i] - Mn) * kL2e);
+        l[h] += w;
+        acc[h] = fmaf(w, O[h][i], acc[h]);
+      }
+      M[h] = Mn;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    if (nan[h]) {
+      val[h] = NAN;
+      lse[h] = NAN;
+    } else if (M[h] == -INFINITY) {
+      val[h] = 0.0f;
+      lse[h] = -INFINITY;
+    } else {
+      val[h] = acc[h] / l[h];
+      lse[h] = M[h] + logf(l[h]);
+    }
+  }
+}
+
 // UNIFIED: FlashDecoding++'s asynchronised softmax with a unified maximum value
 // ("【FlashAttention-V4，非官方】FlashDecoding++", sections 1 and 3). Every head's logits are
 // exponentiated against the preset phi, so a tile needs no maximum at all: one OR over the
 // threads tells whether any logit lies above phi + 60 (natural-log units), or, on a unit's
 // first tile, whether a head lies wholly below phi - 60. Only then is the tile's maximum
 // taken, the reference moved as in the CUDA-core kernel and the event counted.
-template <int G, bool UNIFIED>
+//
+// CASCADE: the launch follows the shared-prefix kernel of a cascade (a.pre_o is set) and
+// each final row merges the prefix's chunk states into its own.
+template <int G, bool UNIFIED, bool CASCADE>
 __global__ void __launch_bounds__(THREADS, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, const DecodeArgs a, int n_units) {
@@ -203,6 +295,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   auto bar = [&](int i) { return sb + SM_BAR + 8 * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = a.wait_limit_ns;
+  // one split per sequence: hand out the longest sequences' units first
+  const bool lpt = a.num_splits == 1 && a.batch > 1 && a.batch <= LPT_MAX;
+  int* hist = reinterpret_cast<int*>(smem + SM_HIST);
+  uint16_t* ord_s = reinterpret_cast<uint16_t*>(smem + SM_ORD);
+  const int my_bucket = lpt && threadIdx.x < a.batch ? lpt_bucket(a, threadIdx.x) : 0;
+  if (lpt && threadIdx.x < LPT_BUCKETS) hist[threadIdx.x] = 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
@@ -231,6 +329,44 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = misc->tmem_base;
   const NextRing ring{smem_u32(&misc->next[0]), bar(B_NF), bar(B_NE)};
+  if (lpt) {
+    // Stable counting sort of the sequences by tiles, most first. Every CTA must arrive at
+    // the same order (a unit id means the same sequence in all of them), so the counts are
+    // taken with atomics but the places are given by one warp in sequence order.
+    uint8_t* bk = smem + SM_BK;
+    for (int b = threadIdx.x; b < a.batch; b += THREADS) {
+      const int key = b == threadIdx.x ? my_bucket : lpt_bucket(a, b);
+      bk[b] = (uint8_t)key;
+      atomicAdd(&hist[key], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      {  // exclusive prefix sum of the 64 counts, two per lane
+        const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
+        int incl = h0 + h1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        hist[2 * lane] = incl - h0 - h1;
+        hist[2 * lane + 1] = incl - h1;
+      }
+      __syncwarp();
+      for (int b0 = 0; b0 < a.batch; b0 += 32) {
+        const int b = b0 + lane;
+        const bool v = b < a.batch;
+        const int key = v ? bk[b] : LPT_BUCKETS + lane;  // lanes past the batch match nobody
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        if (v) ord_s[hist[key] + __popc(same & ((1u << lane) - 1u))] = (uint16_t)b;
+        __syncwarp();
+        if (v && lane == 31 - __clz(same)) hist[key] += __popc(same);  // the group's last lane
+        __syncwarp();
+      }
+    }
+    __syncthreads();
+  }
+  const uint16_t* ord = lpt ? ord_s : nullptr;
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA producers
@@ -245,7 +381,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     uint32_t cnt = 0, qi = 0, k = 0, n_req = 0;
     bool ok = true;
     for (int id = blockIdx.x; ok && id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
-      const Unit u = make_unit(a, id);
+      const Unit u = make_unit(a, id, ord);
       if (u.kind == 0 && !v_role) {
         // Q of the group (rows past the group read other heads' q, or 0 past the last head)
         const uint32_t qb = qi & 1;
@@ -367,7 +503,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       return true;
     };
     for (int id = blockIdx.x; ok && id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
-      const Unit u = make_unit(a, id);
+      const Unit u = make_unit(a, id, ord);
       if (u.kind != 0) continue;
       const uint32_t qb = qi & 1;
       if (!warp_wait(bar(B_QF + qb), (qi >> 1) & 1, lim)) {
@@ -423,7 +559,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     uint32_t g = 0, v_cnt = 0, qi = 0, k = 0, n_fb = 0;
     bool ok = true;
     for (int id = blockIdx.x; id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
-      const Unit u = make_unit(a, id);
+      const Unit u = make_unit(a, id, ord);
       if (u.kind != 0 || !ok) continue;  // the epilogue warps write the rows of the other units
       const uint32_t qb = qi & 1;
       float M[G], lp[G];
@@ -582,16 +718,35 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const float* stats = reinterpret_cast<const float*>(smem + SM_ST);
     uint32_t qi = 0, k = 0;
     bool ok = true;
+    bool pre_ready = !CASCADE;  // cascade: the prefix kernel's results may be read
+    auto wait_prefix = [&]() {
+      if (!pre_ready) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        pre_ready = true;
+      }
+    };
     for (int id = blockIdx.x; id < n_units; id = next_item(ring, k++, n_units, a.err_flag)) {
-      const Unit u = make_unit(a, id);
+      const Unit u = make_unit(a, id, ord);
       const size_t row0 = (size_t)u.b * a.n_qo_heads + (size_t)u.hk * G;  // the group's first row
       if (u.kind == 1 || u.kind == 2) {
         const float o = u.kind == 1 ? NAN : 0.0f, l = u.kind == 1 ? NAN : -INFINITY;
         if (u.kind == 1 && t == 0) set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+        float vals[G], lses[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) out[(row0 + h) * TD + t] = __float2bfloat16_rn(o);
-        if (a.lse && t < G) a.lse[row0 + t] = l;
+        for (int h = 0; h < G; ++h) {
+          vals[h] = o;
+          lses[h] = l;
+        }
+        if (CASCADE && u.kind == 2) {  // no suffix keys: the prefix alone
+          wait_prefix();
+          cascade_merge_group<G>(a, row0, t, vals, lses);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          out[(row0 + h) * TD + t] = __float2bfloat16_rn(vals[h]);
+          if (a.lse && t == h) a.lse[row0 + h] = lses[h];
+        }
         continue;
       }
       if (u.kind != 0) continue;
@@ -621,10 +776,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         good = ok && *reinterpret_cast<volatile int*>(&misc->bad_item[k % NBADM]) != id;
         if (!ok && lane == 0) set_err(a.err_flag, PKV_DEVERR_TIMEOUT);
       }
+      float vals[G], lses[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float val = good ? o[h] / lh[h] : NAN;
-        const float lse = good ? (mh[h] + log2f(lh[h])) * kLn2 : NAN;
+        vals[h] = good ? o[h] / lh[h] : NAN;
+        lses[h] = good ? (mh[h] + log2f(lh[h])) * kLn2 : NAN;
+      }
+      if (CASCADE && u.final_write) {
+        wait_prefix();
+        cascade_merge_group<G>(a, row0, t, vals, lses);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float val = vals[h], lse = lses[h];
         const size_t row = row0 + h;
         if (u.final_write) {
           static_cast<__nv_bfloat16*>(a.out)[row * TD + t] = __float2bfloat16_rn(val);
@@ -655,7 +819,7 @@ bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* di
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int G, bool UNIFIED>
+template <int G, bool UNIFIED, bool CASCADE>
 int launch_tc(const DecodeArgs& a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   {
@@ -675,12 +839,27 @@ int launch_tc(const DecodeArgs& a, cudaStream_t stream) {
       return check_launch(cudaErrorInvalidValue);
   }
   static FuncConfigured configured;
-  if (!configured.ensure(reinterpret_cast<const void*>(decode_tc_kernel<G, UNIFIED>), SMEM)) return PKV_ERR_LAUNCH;
+  if (!configured.ensure(reinterpret_cast<const void*>(decode_tc_kernel<G, UNIFIED, CASCADE>), SMEM)) return PKV_ERR_LAUNCH;
   const long n_units = (long)a.num_splits * a.n_kv_heads * a.batch;
   if (n_units <= 0) return PKV_OK;
   if (n_units > 0x7fffffffL) return PKV_ERR_UNSUPPORTED;
-  decode_tc_kernel<G, UNIFIED><<<(unsigned)n_units, THREADS, SMEM, stream>>>(mq, mk, mv, a, (int)n_units);
-  return check_launch(cudaGetLastError());
+  if (!CASCADE) {
+    decode_tc_kernel<G, UNIFIED, CASCADE><<<(unsigned)n_units, THREADS, SMEM, stream>>>(mq, mk, mv, a, (int)n_units);
+    return check_launch(cudaGetLastError());
+  }
+  // cascade: may start while the prefix kernel before it finishes (it waits for that grid
+  // before reading the prefix's partial states)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)n_units, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return check_launch(cudaLaunchKernelEx(&cfg, decode_tc_kernel<G, UNIFIED, CASCADE>, mq, mk, mv, a, (int)n_units));
 }
 
 }  // namespace
@@ -692,8 +871,14 @@ bool decode_tc_supported(const DecodeArgs& a) {
 
 int launch_decode_tc(const DecodeArgs& a, cudaStream_t stream) {
   const int G = a.n_qo_heads / a.n_kv_heads;
-  if (G == 4) return a.unified ? launch_tc<4, true>(a, stream) : launch_tc<4, false>(a, stream);
-  if (G == 8) return a.unified ? launch_tc<8, true>(a, stream) : launch_tc<8, false>(a, stream);
+  if (a.pre_o) {  // the suffix of a cascade (exact softmax only)
+    if (a.unified) return PKV_ERR_UNSUPPORTED;
+    if (G == 4) return launch_tc<4, false, true>(a, stream);
+    if (G == 8) return launch_tc<8, false, true>(a, stream);
+    return PKV_ERR_UNSUPPORTED;
+  }
+  if (G == 4) return a.unified ? launch_tc<4, true, false>(a, stream) : launch_tc<4, false, false>(a, stream);
+  if (G == 8) return a.unified ? launch_tc<8, true, false>(a, stream) : launch_tc<8, false, false>(a, stream);
   return PKV_ERR_UNSUPPORTED;
 }
 

@@ -42,7 +42,16 @@ struct DecodeArgs {
   // every bounded wait gives up after wait_limit_ns.
   int stall_page = -1;
   uint64_t wait_limit_ns = 2000000000ull;  // the default limit of every bounded wait
+  // Cascade (tensor-core decode only): the shared prefix's fp32 partial states, pre_n chunks
+  // of O [pre_n][batch][n_qo_heads][head_dim] and LSE [pre_n][batch][n_qo_heads], written by
+  // the kernel launched just before on the same stream. Each sequence (one split) merges them
+  // with its own state and writes the final rows; the launch overlaps the prefix kernel's end
+  // (programmatic dependent launch) and waits for it before reading these.
+  const float* pre_o = nullptr;
+  const float* pre_lse = nullptr;
+  int pre_n = 0;
 };
+
 
 // The stall injection that decode launches pick up (process-wide; off by default).
 void decode_stall_settings(int* page, uint64_t* wait_limit_ns);
@@ -125,6 +134,8 @@ int cascade_prefix_chunks(int prefix_len, int page_size, int n_requests, int n_q
                           int n_kv_heads);
 SplitPlan cascade_suffix_plan(int n_requests, int max_suffix_blocks, int n_qo_heads,
                               int n_kv_heads, int head_dim, int dtype);
+// True when the cascade's suffix runs on the tensor-core decode and merges the prefix there.
+bool cascade_uses_tc(int n_qo_heads, int n_kv_heads, int head_dim, int page_size, int dtype);
 int launch_cascade_prefix(const CascadeArgs& a, cudaStream_t stream);
 
 struct ChunkArgs {

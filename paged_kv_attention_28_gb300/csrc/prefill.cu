@@ -522,6 +522,11 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = a.n_qo_heads / a.n_kv_heads;
+  if constexpr (!CAUSAL && !CHUNK) {
+    // The cascade's suffix decode, launched after this kernel on the same stream, may start
+    // now: it streams its own pages and waits for this grid before reading its results.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {

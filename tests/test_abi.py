@@ -61,14 +61,16 @@ def test_split_planning(b):
 def test_workspace_size(b):
     assert b.decode_workspace_size(1, 16, 8, 8, 64, 16, 1) == 0
     # the query and the planner agree for both dtypes
+    # layout: partial O [rows][S][D] fp32, then partial LSE [rows][S] fp32 on a 256-byte boundary
+    up = lambda x: (x + 255) // 256 * 256
     for dt in (b.PKV_F32, b.PKV_BF16):
         s = b.decode_num_splits(16, 256, 32, 32, 128, 16, 0, dt)
         n = b.decode_workspace_size(16, 256, 32, 32, 128, 16, 0, dt)
         rows = 16 * 32
-        assert n == (0 if s == 1 else rows * s * 128 * 4 + ((rows * s * 4 + 255) // 256) * 256)
+        assert n == (0 if s == 1 else rows * s * 128 * 4 + up(rows * s * 4))
     n = b.decode_workspace_size(4, 2048, 32, 8, 128, 16, 32)
     rows = 4 * 32
-    assert n == rows * 32 * 128 * 4 + ((rows * 32 * 4 + 255) // 256) * 256
+    assert n == rows * 32 * 128 * 4 + up(rows * 32 * 4)
     with pytest.raises(b.AttnError):
         b.decode_workspace_size(1, 0, 8, 8, 64, 16, 1)
     with pytest.raises(b.AttnError):

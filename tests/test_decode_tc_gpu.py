@@ -66,6 +66,29 @@ def test_tc_decode_matches_oracle(b, G, splits):
     assert np.all(out[10] == 0) and np.all(lse[10] == -np.inf)   # the empty sequence
 
 
+def test_tc_decode_one_split_longest_first_large_batch(b):
+    """One split per sequence: the kernel hands out the sequences' units longest first (a
+    counting sort in every CTA). 400 sequences (more than one per thread of the sort) of
+    random lengths, including empty ones, one over the table's capacity and lengths past the
+    last bucket; every row against the oracle."""
+    rng = np.random.default_rng(681)
+    lens = rng.integers(0, 700, size=400)
+    lens[::37] = 0
+    lens[5] = 8200                                   # 65 tiles: shares the first bucket
+    case = workloads.make_paged_decode(681, 400, 8, 2, 128, 16, lens.tolist(),
+                                       max_blocks=520, dtype="bf16")
+    bad = case.kv_lens.clone()
+    bad[7] = 520 * 16 + 1                            # above the table's capacity
+    out, lse, err = run(b, case, 1, lens=bad)
+    assert err & b.PKV_DEVERR_BAD_LEN
+    assert np.isnan(out[7]).all() and np.isnan(lse[7]).all()
+    keep = [i for i in range(400) if i != 7]
+    want = ref(case, rows=[(bb, h) for bb in keep for h in range(8)], lens=bad)
+    assert_close(out[keep], want[0][keep], "bf16", "longest-first out")
+    assert_close(lse[keep], want[1][keep], "bf16", "longest-first lse")
+    assert np.all(out[0] == 0) and np.all(lse[0] == -np.inf)   # an empty sequence
+
+
 def test_tc_decode_wide_logits_move_the_max(b):
     """Keys scaled by 4 spread the logits so that later tiles raise the reference max."""
     case = workloads.make_paged_decode(640, 3, 32, 8, 128, 16, [3000, 900, 4096], num_pages=700,
