@@ -4,34 +4,51 @@
 
 namespace pkv {
 
-// Combines the live splits of each (sequence, query head) row by log-sum-exp
-// (merge_row_warp). Rows whose sequence fits in one split were written by the
-// decode kernel and are skipped here. One warp per row, eight rows per CTA.
-constexpr int kMergeWarps = 8;
+// Combines the live splits of each (sequence, query head) row by log-sum-exp, one CTA of
+// kMergeWarps warps per row (merge_row_cta): with up to 8 kMergeWarps splits every load of
+// the row is in flight at once, so a row costs about one round trip to L2, where the
+// decode kernel's partial states still are. Rows whose sequence fits in one split were
+// written by the decode kernel and are skipped here.
+constexpr int kMergeWarps = 4;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_splits_kernel(const DecodeArgs a) {
-  const int row = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  if (row >= a.batch * a.n_qo_heads) return;
+  __shared__ float sm[kMergeWarps * (D + 3)];
+  const int row = blockIdx.x;
   const int b = row / a.n_qo_heads;
   const int P = a.page_size;
-  const int L = __ldg(a.kv_lens + b);
+  const int L = __ldg(a.kv_lens + b);  // an input of the decode kernel, not one of its results
+  // Launched as a programmatic dependent of the decode kernel: wait until that grid has
+  // finished and its partial states are visible. Every CTA waits, so that this grid never
+  // ends before the decode grid.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (L < 0 || L > a.max_blocks * P) return;  // the decode kernel wrote NaN
   const int nblk = (L + P - 1) / P;
   const int n_live = (nblk + a.pages_per_split - 1) / a.pages_per_split;
   if (n_live < 2) return;
   const float* pl = a.part_lse + (size_t)row * a.num_splits;
   const float* po = a.part_o + (size_t)row * a.num_splits * D;
-  merge_row_warp<T, D>(
-      n_live, [&](int i) { return pl[i]; }, [&](int i) { return po + (size_t)i * D; },
-      static_cast<T*>(a.out) + (size_t)row * D, a.lse ? a.lse + row : nullptr);
+  merge_row_cta<T, D, kMergeWarps>(
+      n_live, [&](int i) { return __ldcg(pl + i); }, [&](int i) { return po + (size_t)i * D; },
+      static_cast<T*>(a.out) + (size_t)row * D, a.lse ? a.lse + row : nullptr, sm);
 }
 
 template <typename T, int D>
 int launch_merge_t(const DecodeArgs& a, cudaStream_t stream) {
   const int rows = a.batch * a.n_qo_heads;
-  merge_splits_kernel<T, D><<<(rows + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, stream>>>(a);
-  return check_launch(cudaGetLastError());
+  // Programmatic dependent launch: the merge's CTAs are placed while the decode grid's last
+  // CTAs still run, and read each row's sequence length before the decode grid ends.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)rows, 1, 1);
+  cfg.blockDim = dim3(kMergeWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return check_launch(cudaLaunchKernelEx(&cfg, merge_splits_kernel<T, D>, a));
 }
 
 int launch_merge_splits(const DecodeArgs& a, cudaStream_t stream) {

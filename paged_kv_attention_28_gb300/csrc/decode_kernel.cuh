@@ -281,6 +281,9 @@ decode_paged_kernel(const DecodeArgs a) {
   const int warp = threadIdx.x >> 5;
   const int hh = warp < C::NW ? warp / C::WPH : 0;  // a consumer warp's head within the CTA
   const int g = g0 + hh;
+  // The split merge, launched next on the same stream, may take its place on the SMs once
+  // every CTA of this grid has started; it waits for this grid before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int kv_len = __ldg(a.kv_lens + b);
   if (kv_len < 0 || kv_len > a.max_blocks * P) {

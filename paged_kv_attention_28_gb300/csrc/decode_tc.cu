@@ -367,6 +367,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     __syncthreads();
   }
   const uint16_t* ord = lpt ? ord_s : nullptr;
+  // The split merge, launched next on the same stream, may take its place on the SMs once
+  // every CTA of this grid has started (or was taken over); it waits for this grid before
+  // it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ TMA producers
@@ -807,6 +811,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // cascade: a CTA whose units never read the prefix's states still ends only after the
+  // prefix grid, so that this grid never ends before it
+  if (CASCADE) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,

@@ -119,4 +119,85 @@ __device__ __forceinline__ void merge_row_warp(int n, LseF lse_of, OF o_of, T* o
   if (lse_out && lane == 0) *lse_out = M + logf(l);
 }
 
+// The same merge by the MW warps of a CTA, for rows with many partials: warp w takes
+// partials w, w + MW, ... eight at a time, all eight loads in flight before any is used,
+// keeps its own running (max, sum, weighted O), and the warps' states are combined through
+// shared memory. For n <= 8 MW every load of the row is issued in one round. Every thread
+// of the CTA calls this with the same arguments; `sm` holds MW * (D + 3) floats.
+template <typename T, int D, int MW, typename LseF, typename OF>
+__device__ __forceinline__ void merge_row_cta(int n, LseF lse_of, OF o_of, T* out, float* lse_out, float* sm) {
+  constexpr int DL = D / 32, PER = 8;
+  constexpr float kL2e = 1.4426950408889634f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float m = -INFINITY, l = 0.0f, acc[DL];
+#pragma unroll
+  for (int e = 0; e < DL; ++e) acc[e] = 0.0f;
+  bool bad = false;
+  for (int base = warp; base < n; base += MW * PER) {
+    float w[PER], x[PER][DL];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = base + k * MW;
+      if (i < n) {
+        w[k] = lse_of(i);
+        load_cols<DL>(o_of(i) + lane * DL, x[k]);
+      } else {
+        w[k] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) x[k][e] = 0.0f;
+      }
+    }
+    float mn = m;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      bad |= w[k] != w[k];
+      mn = fmaxf(mn, w[k]);
+    }
+    if (mn == -INFINITY) continue;
+    const float sc = ex2((m - mn) * kL2e);  // 0 while m = -inf
+    l *= sc;
+#pragma unroll
+    for (int e = 0; e < DL; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const float wk = ex2((w[k] - mn) * kL2e);  // 0 for the slots past n
+      l += wk;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) acc[e] = fmaf(wk, x[k][e], acc[e]);
+    }
+    m = mn;
+  }
+  float* s_acc = sm;               // [MW][D]
+  float* s_m = sm + MW * D;        // [MW]
+  float* s_l = s_m + MW;           // [MW]
+  float* s_bad = s_l + MW;         // [MW]
+#pragma unroll
+  for (int e = 0; e < DL; ++e) s_acc[warp * D + lane * DL + e] = acc[e];
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
+    s_bad[warp] = bad ? 1.0f : 0.0f;
+  }
+  __syncthreads();
+  float M = -INFINITY, nan_seen = 0.0f;
+#pragma unroll
+  for (int v = 0; v < MW; ++v) {
+    M = fmaxf(M, s_m[v]);
+    nan_seen += s_bad[v];
+  }
+  float sc[MW], L = 0.0f;
+#pragma unroll
+  for (int v = 0; v < MW; ++v) {
+    sc[v] = M == -INFINITY ? 0.0f : ex2((s_m[v] - M) * kL2e);
+    L = fmaf(sc[v], s_l[v], L);
+  }
+  for (int c = threadIdx.x; c < D; c += MW * 32) {
+    float o = 0.0f;
+#pragma unroll
+    for (int v = 0; v < MW; ++v) o = fmaf(sc[v], s_acc[v * D + c], o);
+    out[c] = merge_cast<T>(nan_seen > 0.0f ? NAN : M == -INFINITY ? 0.0f : o / L);
+  }
+  if (lse_out && threadIdx.x == 0) *lse_out = nan_seen > 0.0f ? NAN : M == -INFINITY ? -INFINITY : M + logf(L);
+}
+
 }  // namespace pkv

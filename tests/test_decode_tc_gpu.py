@@ -89,6 +89,20 @@ def test_tc_decode_one_split_longest_first_large_batch(b):
     assert np.all(out[0] == 0) and np.all(lse[0] == -np.inf)   # an empty sequence
 
 
+@pytest.mark.parametrize("splits", [4, 8])
+def test_tc_decode_many_units_with_idle_splits(b, splits):
+    """64 sequences x 8 KV heads x 4 or 8 splits: thousands of units, so running CTAs take
+    many of them in turn, and short sequences leave most of their splits idle, so a CTA
+    often passes several idle units between two live ones (the pipeline must neither stall
+    nor wait out a bounded wait there). Every row against the oracle."""
+    case = workloads.make_paged_decode(690 + splits, 64, 32, 8, 128, 16, (16, 1024), dtype="bf16")
+    out, lse, err = run(b, case, splits)
+    assert err == 0
+    want = ref(case)
+    assert_close(out, want[0], "bf16", f"idle splits S={splits} out")
+    assert_close(lse, want[1], "bf16", f"idle splits S={splits} lse")
+
+
 def test_tc_decode_wide_logits_move_the_max(b):
     """Keys scaled by 4 spread the logits so that later tiles raise the reference max."""
     case = workloads.make_paged_decode(640, 3, 32, 8, 128, 16, [3000, 900, 4096], num_pages=700,
