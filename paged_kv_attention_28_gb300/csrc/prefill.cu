@@ -113,7 +113,7 @@ struct TileArgs {
   int32_t* err_flag;
   float scale;
   int batch, seq_len, n_qo_heads, n_kv_heads;
-  int group_bh, tail_bh;  // causal item order (make_item)
+  int group_bh, tail_bh;  // causal and chunk item order (grouped_order)
   // shared prefix
   const int32_t* prefix_table;
   int prefix_len, n_prefix_pages, n_requests, num_pages;
@@ -189,6 +189,29 @@ struct Item {
   int id;        // the item's index in the grid
 };
 
+// Item order for work made of `units` units (a (b, h) or (b, KV head)) of n_pairs query-tile
+// pairs each, pair n_pairs - 1 the longest (CTAs take items in index order): the units but
+// the last `tail` go in groups of `group`, each group's pairs longest first, so that the
+// pairs reading the same K/V run at about the same time and find it in L2; the last `tail`
+// units go longest first over all their pairs, so the grid ends on short items.
+__device__ __forceinline__ void grouped_order(int id, int units, int n_pairs, int group, int tail_units,
+                                              int& pr, int& unit) {
+  const int tail = min(units, tail_units);
+  const int head_items = (units - tail) * n_pairs;
+  if (id < head_items) {
+    const int per_group = group * n_pairs;
+    const int gi = id / per_group;
+    const int gsz = min(group, (units - tail) - gi * group);
+    const int rr = id - gi * per_group;
+    pr = n_pairs - 1 - rr / gsz;
+    unit = gi * group + rr % gsz;
+  } else {
+    const int rr = id - head_items;
+    pr = n_pairs - 1 - rr / tail;
+    unit = (units - tail) + rr % tail;
+  }
+}
+
 template <bool CAUSAL, bool CHUNK = false>
 __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
   Item it{};
@@ -196,14 +219,15 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
   const int H = a.n_qo_heads;
   const int G = a.n_qo_heads / a.n_kv_heads;
   if constexpr (CHUNK) {
-    // Items (query-tile pair, KV head, sequence), the pairs with the most key tiles first.
+    // Items (query-tile pair, KV head, sequence) in grouped_order over the (sequence, KV
+    // head) units: every pair of a unit reads the unit's whole prefix, so a unit's pairs run
+    // at about the same time and the prefix's K/V comes from L2 after the first.
     // A tile is 128/G new tokens x the G query heads of one KV head.
     const int TPT = BM / G;  // tokens per tile
     const int n_qt = (a.chunk_len + TPT - 1) / TPT;
     const int n_pairs = (n_qt + 1) / 2;
-    const int per_pr = a.batch * a.n_kv_heads;
-    const int pr = n_pairs - 1 - id / per_pr;
-    const int rem = id % per_pr;
+    int pr, rem;
+    grouped_order(id, a.batch * a.n_kv_heads, n_pairs, a.group_bh, a.tail_bh, pr, rem);
     const int hk = rem % a.n_kv_heads;
     const int b = rem / a.n_kv_heads;
     int L0 = __ldg(a.prefix_lens + b);
@@ -224,28 +248,10 @@ __device__ __forceinline__ Item make_item(const TileArgs& a, int id) {
   } else if constexpr (CAUSAL) {
     const int n_qt = (a.seq_len + BM - 1) / BM;
     const int n_pairs = (n_qt + 1) / 2;
-    // Longest first: the pairs nearest the end of the sequence have the most key tiles.
-    // Item order (CTAs take items in index order): the (b, h) pairs but the last tail_bh
-    // go in groups of group_bh, each group's query-tile pairs longest first, so that the
-    // pairs reading the same K/V run at about the same time and find it in L2; the last
-    // tail_bh (b, h) go longest first over all their pairs, so the grid ends on short
-    // items.
-    const int MBH = H * a.batch;
-    const int tail = min(MBH, a.tail_bh);
-    const int head_items = (MBH - tail) * n_pairs;
+    // Items in grouped_order over the (b, h) units; the pairs nearest the end of the
+    // sequence have the most key tiles.
     int pr, rem;
-    if (id < head_items) {
-      const int per_group = a.group_bh * n_pairs;
-      const int gi = id / per_group;
-      const int gsz = min(a.group_bh, (MBH - tail) - gi * a.group_bh);
-      const int rr = id - gi * per_group;
-      pr = n_pairs - 1 - rr / gsz;
-      rem = gi * a.group_bh + rr % gsz;
-    } else {
-      const int rr = id - head_items;
-      pr = n_pairs - 1 - rr / tail;
-      rem = (MBH - tail) + rr % tail;
-    }
+    grouped_order(id, H * a.batch, n_pairs, a.group_bh, a.tail_bh, pr, rem);
     const int h = rem % H;
     const int b = rem / H;
     const int qtA = 2 * pr;
@@ -1018,6 +1024,14 @@ int launch_prefill_chunk(const ChunkArgs& c, cudaStream_t stream) {
   const long tpt = BM / G;
   const long n_qt = (c.chunk_len + tpt - 1) / tpt;
   const long grid = (n_qt + 1) / 2 * c.n_kv_heads * c.batch;
+  // The same grouping as the causal prefill: about 64 items per group, a tail of about 1.25
+  // waves of items. Without it the pairs of one (sequence, KV head) ran a wave or more apart
+  // and each re-read the sequence's K/V from DRAM (about 3.7x the algorithmic bytes).
+  const int n_pairs = (int)((n_qt + 1) / 2);
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 148;
+  a.group_bh = 64 / n_pairs > 1 ? 64 / n_pairs : 1;
+  a.tail_bh = (5 * sms / 4 + n_pairs - 1) / n_pairs;
   return launch_tiles<false, true>(mq, mk, mv, a, grid, stream);
 }
 
