@@ -730,6 +730,38 @@ def other_workloads(B, workloads, dev, stream, steps, hbm_peak, parts=OTHER_PART
         entry("single_seq_decode_f32_graph", c.kv_bytes(), ms,
               {"note": "the same call replayed from a CUDA graph captured once; L2 flushed before each replay"})
 
+        # What a graph is for: a model step makes one such call per layer. 32 layers, each
+        # with its own query, outputs and K/V pool, called back to back from Python, against
+        # the same 32 calls captured once and replayed as one graph launch. Timed as a
+        # group (CUDA events around all 32, L2 flushed before the group): the direct calls
+        # also pay the host's per-call launch cost whenever it exceeds the kernel's time.
+        n_layers = 32
+        layers = []
+        for _ in range(n_layers):
+            layers.append((torch.randn_like(q), kp.clone(), vp.clone(), torch.empty_like(q),
+                           torch.empty(q.shape[:2], dtype=torch.float32, device=dev)))
+
+        def all_layers():
+            for ql, kl, vl, ol, ll in layers:
+                B.decode_paged(ql, kl, vl, bt, ln, c.scale, out=ol, lse=ll, workspace=ws)
+
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            all_layers()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph_l = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_l):
+            all_layers()
+        ms_direct = time_calls(all_layers, max(3, steps // 10), stream, dev)
+        ms_graph = time_calls(graph_l.replay, max(3, steps // 10), stream, dev)
+        entry("single_seq_decode_f32_32_layers_direct", n_layers * c.kv_bytes(), ms_direct,
+              {"us_per_layer": 1000 * ms_direct / n_layers,
+               "note": "32 calls (one per layer, own q, out and K/V pool) from Python back to back"})
+        entry("single_seq_decode_f32_32_layers_graph", n_layers * c.kv_bytes(), ms_graph,
+              {"us_per_layer": 1000 * ms_graph / n_layers,
+               "note": "the same 32 calls captured once into a CUDA graph, replayed as one launch"})
+
     return res
 
 def prefill_bench(B, workloads, dev, stream, args, world, bf16_peak, bf16_sust, peak_src):
