@@ -129,13 +129,15 @@ size_t attn_decode_workspace_size(int batch, int max_blocks_per_seq, int n_qo_he
  * One unit of work is (sequence, KV head, split): that split's K/V pages are
  * streamed through the block table into a shared-memory ring, with a running max
  * and sum (online softmax), and a partial (O, LSE) state is written. A merge kernel
- * then combines the partials by log-sum-exp. Sequences whose pages fit in one split
- * are written directly. With 1 or 2 query heads per KV head (and for fp32) the dot
+ * (one CTA per output row, launched on `stream` as a programmatic dependent of the
+ * decode so that it is placed while the decode's last CTAs run) then combines the
+ * partials by log-sum-exp. Sequences whose pages fit in one split are written directly. With 1 or 2 query heads per KV head (and for fp32) the dot
  * products and sums run on the CUDA cores, one CTA per unit, the group's queries in
  * registers. For bf16, head_dim 128 and 4 or 8 query heads per KV head they run on
  * the tcgen05 tensor cores: 128-key tiles (8 pages) against the group's queries,
  * padded to 16, with fp32 accumulators in tensor memory; CTAs take units from the
- * grid until none is left. The workspace (device, >= attn_decode_workspace_size bytes,
+ * grid until none is left, and with one split per sequence (batch <= 2048) the longest
+ * sequences' units are handed out first. The workspace (device, >= attn_decode_workspace_size bytes,
  * 256-byte aligned) holds the partials; its contents on entry do not matter.
  */
 int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
