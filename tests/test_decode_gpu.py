@@ -116,6 +116,19 @@ def test_split_count_invariance(b, splits):
     check(case, got, ref(case), f"splits={splits}")
 
 
+@pytest.mark.parametrize("dtype,head_dim,hq,hkv,splits", [
+    ("f32", 64, 4, 4, 48), ("bf16", 128, 8, 8, 64), ("bf16", 128, 16, 4, 48)])
+def test_many_splits_merge_in_rounds(b, dtype, head_dim, hq, hkv, splits):
+    """More live splits than the merge's four warps take in one round (8 each): 43 to 64
+    partials per row, so every warp loops and the last round is ragged; sequences of one
+    split, of a few and of all are mixed."""
+    case = workloads.make_paged_decode(40 + splits + head_dim, 4, hq, hkv, head_dim, 16,
+                                       [4096, 700, 16, 3001], max_blocks=256, dtype=dtype)
+    got = run(b, case, splits)
+    assert got[2] == 0
+    check(case, got, ref(case), f"{dtype} d{head_dim} {hq}/{hkv} splits={splits}")
+
+
 def test_page_shuffle_invariance_gpu(b):
     case = workloads.make_paged_decode(32, 4, 8, 8, 64, 16, [70, 33, 160, 5], num_pages=40,
                                        dtype="f32")
