@@ -640,6 +640,21 @@ def other_workloads(B, workloads, dev, stream, steps, hbm_peak, parts=OTHER_PART
                                                lse=lse, workspace=ws), steps, stream, dev)
         entry("long_context_gqa8_decode", c.kv_bytes(), ms, {"num_splits": S, "group": 8})
         del q, kp, vp, bt, ln, ws
+        # the GQA-8 batch over FP8 E4M3 pools (the tensor-core path with in-kernel conversion)
+        c = workloads.long_context_gqa8_decode_fp8(poison=False)
+        q, kc, vc, ks, vs, bt, ln = (t.to(dev) for t in (c.q, c.k_codes, c.v_codes, c.k_scale, c.v_scale,
+                                                         c.block_table, c.kv_lens))
+        out = torch.empty_like(q)
+        lse = torch.empty(c.batch, c.n_qo_heads, dtype=torch.float32, device=dev)
+        ws = B.alloc_workspace(B.decode_workspace_size(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads,
+                                                       c.head_dim, 16, S, B.PKV_FP8_E4M3), dev)
+        ms = time_calls(lambda: B.decode_paged_fp8(q, kc, vc, ks, vs, bt, ln, c.scale, num_splits=S, out=out,
+                                                   lse=lse, workspace=ws), steps, stream, dev)
+        toks = int(c.kv_lens.sum())
+        entry("long_context_gqa8_decode_fp8", c.kv_bytes(), ms,
+              {"num_splits": S, "group": 8, "tokens_per_s": toks / (ms / 1e3),
+               "bytes_note": "E4M3 codes of every token's K and V plus the scales of the pages read"})
+        del q, kc, vc, ks, vs, bt, ln, ws
 
     if "cascade" in parts:
         c = workloads.cascade_shared_prefix_decode(poison=False)

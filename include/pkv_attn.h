@@ -231,9 +231,13 @@ int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void
  * tile's V scale enters the V sum as an f16 value (11-bit significand, normal from 2^-14
  * to 65504): V scales above 65504 are not supported, and below about 2^-14 such a weight
  * keeps an absolute precision of 2^-24. Pools
- * must be 16-byte aligned. A CTA takes two adjacent KV heads, so n_kv_heads must be
- * even. Built for head_dim 64 and 128, page_size 16 and GQA groups 1, 2, 4 and 8;
- * other shapes return PKV_ERR_UNSUPPORTED.
+ * must be 16-byte aligned, and n_kv_heads must be even (the CUDA-core kernel's CTA takes two
+ * adjacent KV heads). Built for head_dim 64 and 128, page_size 16 and GQA groups 1, 2, 4 and
+ * 8; other shapes return PKV_ERR_UNSUPPORTED. At head_dim 128 with 4 or 8 query heads per KV
+ * head the products run on the tcgen05 tensor cores: converter warps take each tile's codes
+ * to f16 in shared memory (exactly), q goes to f16 as above, the K scale multiplies each
+ * logit and a weight times its page's V scale enters the V product as f16, with fp32
+ * accumulation; the other shapes run on the CUDA cores.
  */
 int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_pages,
                           const float* k_scale, const float* v_scale, const int32_t* block_table,

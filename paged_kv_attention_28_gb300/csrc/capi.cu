@@ -85,6 +85,28 @@ SplitPlan plan_decode_splits(int batch, int max_blocks, int n_kv_heads, int requ
   return SplitPlan{(max_blocks + pps - 1) / pps, pps};
 }
 
+// The split plan of a decode call, the same for the call and for the size queries. E4M3
+// pools at head_dim 128 (page 16, groups of 1, 2, 4 or 8) run on the tensor-core decode and
+// are planned as the bf16 ones; the others on the CUDA-core kernel, whose E4M3 CTA takes two
+// KV heads.
+static SplitPlan plan_decode(int batch, int max_blocks, int n_qo_heads, int n_kv_heads, int head_dim, int page_size,
+                      int num_splits, int dtype) {
+  const int G = n_qo_heads / n_kv_heads;
+  if (dtype == PKV_FP8_E4M3) {
+    DecodeArgs d{};
+    d.n_qo_heads = n_qo_heads;
+    d.n_kv_heads = n_kv_heads;
+    d.head_dim = head_dim;
+    d.page_size = page_size;
+    d.dtype = PKV_BF16;
+    d.fp8 = true;
+    if (decode_tc_supported(d))
+      return plan_decode_splits(batch, max_blocks, n_kv_heads, num_splits, decode_ctas_per_sm(PKV_BF16, head_dim, G));
+    return plan_decode_splits(batch, max_blocks, n_kv_heads / 2, num_splits, decode_ctas_per_sm(dtype, head_dim, G));
+  }
+  return plan_decode_splits(batch, max_blocks, n_kv_heads, num_splits, decode_ctas_per_sm(dtype, head_dim, G));
+}
+
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Split partials: O [rows][S][D], LSE [rows][S].
@@ -133,9 +155,8 @@ static int decode_common(const DecodeCall& c, bool unified, float phi, int32_t* 
   if (!decode_supported(c.dtype, c.head_dim, c.page_size, G)) return PKV_ERR_UNSUPPORTED;
   if (c.batch > 65535 || c.n_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (fp8 && c.n_kv_heads % 2) return PKV_ERR_UNSUPPORTED;  // two KV heads per CTA
-  const SplitPlan plan = plan_decode_splits(c.batch, c.max_blocks, fp8 ? c.n_kv_heads / 2 : c.n_kv_heads,
-                                            c.num_splits,
-                                            decode_ctas_per_sm(fp8 ? PKV_FP8_E4M3 : c.dtype, c.head_dim, G));
+  const SplitPlan plan = plan_decode(c.batch, c.max_blocks, c.n_qo_heads, c.n_kv_heads, c.head_dim, c.page_size,
+                                     c.num_splits, fp8 ? PKV_FP8_E4M3 : c.dtype);
   const size_t need = decode_ws_bytes(c.batch, c.n_qo_heads, c.n_kv_heads, c.head_dim, plan.num_splits);
   if (need > 0 && (!c.workspace || c.workspace_bytes < need ||
                    (reinterpret_cast<uintptr_t>(c.workspace) & 255u) != 0))
@@ -209,10 +230,7 @@ int attn_decode_num_splits(int batch, int max_blocks_per_seq, int n_qo_heads, in
     return PKV_ERR_INVALID_ARG;
   if (dtype != PKV_F32 && dtype != PKV_BF16 && dtype != PKV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
   if (dtype == PKV_FP8_E4M3 && n_kv_heads % 2) return PKV_ERR_UNSUPPORTED;
-  // the FP8 kernel's CTA takes two KV heads
-  return plan_decode_splits(batch, max_blocks_per_seq, dtype == PKV_FP8_E4M3 ? n_kv_heads / 2 : n_kv_heads,
-                            num_splits,
-                            decode_ctas_per_sm(dtype, head_dim, n_qo_heads / n_kv_heads))
+  return plan_decode(batch, max_blocks_per_seq, n_qo_heads, n_kv_heads, head_dim, page_size, num_splits, dtype)
       .num_splits;
 }
 

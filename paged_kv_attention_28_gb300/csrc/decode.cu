@@ -100,8 +100,8 @@ int launch_decode_partials(const DecodeArgs& a, cudaStream_t stream) {
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  const int rc = a.fp8                    ? dispatch_decode_fp8(a, stream)
-                 : decode_tc_supported(a) ? launch_decode_tc(a, stream)
+  const int rc = decode_tc_supported(a) ? launch_decode_tc(a, stream)
+                 : a.fp8                  ? dispatch_decode_fp8(a, stream)
                  : a.unified              ? dispatch_decode_unified(a, stream)
                                           : dispatch_decode<false>(a, stream);
   if (rc != PKV_OK) return rc;

@@ -505,6 +505,13 @@ def long_context_gqa8_decode(poison: bool = True) -> PagedDecodeCase:
                              name="long_context_gqa8_decode")
 
 
+def long_context_gqa8_decode_fp8(poison: bool = True) -> PagedDecodeFp8Case:
+    """The same long-context GQA-8 batch over FP8 E4M3 pools with per-(page, KV head) scales."""
+    return make_paged_decode_fp8(1014, 4, 64, 8, 128, 16, [32768] * 4, num_pages=8192,
+                                 max_blocks=2048, k_std=2.0, poison=poison,
+                                 name="long_context_gqa8_decode_fp8")
+
+
 LONG_CONTEXT_SPLITS = 32
 
 

@@ -83,8 +83,9 @@ def test_decode_fp8_wide_scales_and_logits(b):
         check(got, want, f"fp8 wide splits={splits}")
 
 
-def test_decode_fp8_bad_page_sets_flag(b):
-    c = workloads.make_paged_decode_fp8(72, 3, 4, 2, 64, 16, [40, 40, 40], num_pages=12, max_blocks=4)
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_decode_fp8_bad_page_sets_flag(b, head_dim):
+    c = workloads.make_paged_decode_fp8(72, 3, 4, 2, head_dim, 16, [40, 40, 40], num_pages=12, max_blocks=4)
     table = c.block_table.clone()
     table[1, 1] = c.num_pages + 5               # out of range, inside the sequence
     table[2, 3] = 10**6                         # out of range but past the length: never read
@@ -94,6 +95,18 @@ def test_decode_fp8_bad_page_sets_flag(b):
         assert np.isnan(out[1]).all() and np.isnan(lse[1]).all()
         want = ref(c, rows=[(bb, h) for bb in (0, 2) for h in range(4)], table=table)
         check((out[[0, 2]], lse[[0, 2]]), (want[0][[0, 2]], want[1][[0, 2]]), "fp8 good rows")
+
+
+def test_decode_fp8_tensor_core_many_units_and_idle_splits(b):
+    """head_dim 128 runs on the tensor cores: 48 sequences x 4 KV heads x 6 splits, so CTAs
+    take many units in turn, with short sequences leaving most splits idle; and one split
+    per sequence (the longest-first order). Every row against the oracle."""
+    c = workloads.make_paged_decode_fp8(74, 48, 16, 4, 128, 16, (1, 1500), k_std=2.0)
+    want = ref(c)
+    for splits in (6, 1):
+        got = run(b, c, splits)
+        assert got[2] == 0
+        check(got, want, f"fp8 tensor cores splits={splits}")
 
 
 def test_decode_fp8_rejects_missing_scales(b):
@@ -120,3 +133,36 @@ def test_fp8_query_far_outside_f16_range(b, q_mag, G):
     got = run(b, c, 2)
     assert got[2] == 0
     check(got, ref(c), f"fp8 q magnitude {q_mag} G={G}")
+
+
+def test_long_context_gqa8_fp8_split32_sampled_rows(b):
+    """The long-context batch with 8 query heads per KV head over E4M3 pools (the tensor-core
+    path, codes converted to f16 in shared memory), 32 splits: every head of 6 KV groups
+    against the oracle, and all rows finite."""
+    c = workloads.long_context_gqa8_decode_fp8()
+    got = run(b, c, 32)
+    assert got[2] == 0
+    rows = [(bb, h) for bb, g in [(0, 0), (1, 3), (2, 7), (3, 5), (0, 6), (3, 1)] for h in range(8 * g, 8 * g + 8)]
+    want = ref(c, rows=rows)
+    idx = tuple(np.array(rows).T)
+    check((got[0][idx], got[1][idx]), (want[0][idx], want[1][idx]), "fp8 gqa8 sampled")
+    assert np.isfinite(got[0]).all() and np.isfinite(got[1]).all()
+
+
+def test_fp8_tensor_core_stalled_wait_is_reported_and_gpu_stays_usable(b):
+    """The stall hook withholds the K copies of the tile holding page 9 of each split on the
+    E4M3 tensor-core path (4 query heads per KV head): the converters' bounded wait runs out,
+    the kernel reports it and writes the affected rows as NaN; the next call matches."""
+    c = workloads.make_paged_decode_fp8(661, 3, 8, 2, 128, 16, [300, 20, 520], num_pages=80)
+    want = ref(c)
+    b.debug_decode_stall(9, 200_000)
+    try:
+        out, lse, err = run(b, c, 1)
+    finally:
+        b.debug_decode_stall(-1)
+    assert err & b.PKV_DEVERR_TIMEOUT
+    assert np.isnan(out[[0, 2]]).all() and np.isnan(lse[[0, 2]]).all()   # 19 and 33 pages
+    got = run(b, c, 1)
+    assert got[2] == 0
+    check(got, want, "fp8 after a timed-out launch")
+
