@@ -30,6 +30,10 @@
 // (columns 32..47 and 48..63).
 // Shared memory: K and V rings of 3 tiles (32 KiB each), Q and P^T double-buffered (4 KiB
 // each), a small reduction area, the barriers, the sequence order.
+//
+// E4M3 pools (groups of 4 and 8): the producers copy tiles of codes into staging rings; warps
+// 11 .. 16 (544 threads) convert them to f16 into K and V rings of 2 tiles, and the products
+// take f16 operands (see produce_fp8 and convert_fp8).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
