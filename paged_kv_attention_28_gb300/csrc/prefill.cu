@@ -60,28 +60,32 @@ constexpr int BS = 64;         // keys per S step (half a K/V tile)
 constexpr int HD = 128;        // head dim
 constexpr int SUB = 16384;     // one 128-row x 64-column bf16 sub-tile (128-byte swizzle)
 constexpr int TILE = 2 * SUB;  // 128 x 128 bf16
-constexpr int NSK = 3;         // K ring stages (a K tile is free once both S products read it)
-constexpr int NSV = 2;         // V ring stages (a V tile is free once both PV products read it)
-constexpr int SM_Q = 0;                      // Q_A, Q_B
-constexpr int SM_K = SM_Q + 2 * TILE;
+constexpr int NSK = 2;         // K ring stages (a K tile is free once both S products read it)
+constexpr int NSV = 3;         // V ring stages (a V tile is free once both PV products read it)
+constexpr int kReqAhead = 1;   // K tiles of an item still to copy when the next item is requested
+constexpr int NQ = 2;          // Q buffers: Q tile n (item k, tile t: n = 2k + t) uses buffer n % NQ
+constexpr int NQB = 2 * NQ;    // q_full / q_empty barriers: tile n uses barrier n % NQB
+constexpr int SM_Q = 0;
+constexpr int SM_K = SM_Q + NQ * TILE;
 constexpr int SM_V = SM_K + NSK * TILE;
 constexpr int SM_BAR = SM_V + NSV * TILE;
-// barriers: q_full[2], k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2 tiles][2
-// buffers], p_full[2][2], o_done[2] (one phase per PV step), drain[2], q_empty[2]
-// (products of an item done with a Q tile), o_free[2] (epilogue read O), o_item[2] (an
-// item's last PV finished). k_empty and v_empty take one arrival from each MMA issuer.
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 4, BAR_VF = 7, BAR_VE = 9, BAR_SF = 11, BAR_PF = 15,
-              BAR_OD = 19, BAR_DRAIN = 21, BAR_QE = 23, BAR_OF = 25, BAR_Q1 = 27, BAR_ST = 28, BAR_IE = 30,
-              BAR_OI = 32, BAR_NF = 34, BAR_NE = 38, BAR_VZ = 42, NBAR = 44;
-// next_full[4] / next_empty[4]: a ring of work-distribution responses (work_queue.cuh);
-// next_full completes when a response lands (16 bytes), next_empty takes one arrival from
-// every warp.
-// q_full and q_empty exist per query tile: tile t's Q uses BAR_Q / BAR_Q1 and BAR_QE + t.
-// st_full[2]: a tile's softmax has written its rows' 1/l for the epilogue warpgroup;
-// inv_empty[2]: the epilogue has read them, so the next item's softmax may overwrite them.
-// v_zeroed (chunk mode): tile B's issuer has zeroed the V rows past the sequence's end in
-// the last key tile that both tiles read (one phase per such item). NBAR stays even so
-// that the structure after the barriers is 16-byte aligned.
+// Barriers. q_full / q_empty: Q tile n uses barrier n % NQB, so each barrier serves one MMA
+// issuer (tile n % 2) in turn and every wait on it is for the phase after the last one that
+// issuer saw. k_full / k_empty, v_full / v_empty: the rings (empty takes one arrival from each
+// MMA issuer). s_full[2 tiles][2 buffers], p_full[2][2]; o_done[2] (one phase per PV step);
+// drain[2]; o_free[2] (the epilogue read O); st_full[2] (a tile's softmax wrote its rows' 1/l
+// for the epilogue warpgroup); inv_empty[2] (the epilogue read them, so the next item's
+// softmax may overwrite them); o_item[2] (an item's last PV finished); next_full[NXS] /
+// next_empty[NXS]: the ring of work-distribution responses (work_queue.cuh), next_full
+// completing when a response lands (16 bytes) and next_empty taking one arrival from every
+// warp; v_zeroed (chunk mode): tile B's issuer has zeroed the V rows past the sequence's end
+// in the last key tile that both tiles read (one phase per such item).
+constexpr int BAR_QF = 0, BAR_QE = BAR_QF + NQB, BAR_KF = BAR_QE + NQB, BAR_KE = BAR_KF + NSK,
+              BAR_VF = BAR_KE + NSK, BAR_VE = BAR_VF + NSV, BAR_SF = BAR_VE + NSV, BAR_PF = BAR_SF + 4,
+              BAR_OD = BAR_PF + 4, BAR_DRAIN = BAR_OD + 2, BAR_OF = BAR_DRAIN + 2, BAR_ST = BAR_OF + 2,
+              BAR_IE = BAR_ST + 2, BAR_OI = BAR_IE + 2, BAR_NF = BAR_OI + 2, BAR_NE = BAR_NF + NXS,
+              BAR_VZ = BAR_NE + NXS;
+constexpr int NBAR = (BAR_VZ + 2) & ~1;  // even, so that what follows is 16-byte aligned
 constexpr int SM_INV = SM_BAR + NBAR * 8;          // float [2 tiles][128 rows]: 1/l per row
 constexpr int SM_MISC = SM_INV + 2 * BM * 4;
 constexpr int SMEM_BYTES = SM_MISC + 128 + 1024;  // + slack to align the base to 1024
@@ -633,14 +637,17 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         };
         for (int id = blockIdx.x; ok && id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
           const Item it = make_item<CAUSAL, CHUNK>(a, id);
-          // Q_t may be replaced once the previous item's last S_t has read it.
+          // Q tile n = 2k + t goes to buffer n % NQ once the products of Q tile n - NQ (the
+          // last one in that buffer) are done.
           auto load_q = [&](int t) -> bool {
-            const uint32_t qf = bar(t == 0 ? BAR_Q : BAR_Q1);
-            if (q_cnt > 0 && !warp_wait(bar(BAR_QE + t), (q_cnt - 1) & 1)) return false;
+            const uint32_t n = q_cnt;
+            const uint32_t qf = bar(BAR_QF + n % NQB);
+            if (n >= NQ && !warp_wait(bar(BAR_QE + (n - NQ) % NQB), ((n - NQ) / NQB) & 1)) return false;
+            ++q_cnt;
             if (elect_one()) {
               mbar_arrive_expect_tx(qf, TILE);
               for (int half = 0; half < 2; ++half) {
-                const uint32_t dst = sb + SM_Q + t * TILE + half * SUB;
+                const uint32_t dst = sb + SM_Q + (n % NQ) * TILE + half * SUB;
                 if constexpr (CHUNK)
                   tma_load_4d(dst, &mq, half * 64, it.hk * G, (t == 0 ? it.A : it.B).q0, it.b, qf);
                 else if constexpr (CAUSAL)
@@ -656,18 +663,30 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             for (int j = 0; ok && j < it.n_kv; ++j) ok = load_tile(it, j, true);
           } else {
             // Q_A, K0, Q_B, K1, K2, ...: both tiles can start as soon as K0 is in.
+            // Ask for the next item just before this one's last kReqAhead K tiles: the
+            // response (which takes about a microsecond) is back by the time tile A could
+            // start the next item, and the CTA holds the next item for as short a time as
+            // that allows.
+            auto request = [&]() {
+              const uint32_t s = k % NXS, u = k / NXS;
+              if (ok && u > 0 && !warp_wait(ring.empty0 + 8 * s, (u - 1) & 1)) ok = false;
+              if (ok) {
+                if (elect_one()) request_next_cta(ring.slot0 + 16 * s, ring.full0 + 8 * s);
+                __syncwarp();
+                ++n_req;
+              }
+            };
             ok = load_q(0) && load_tile(it, 0, false) && load_q(1);
-            for (int j = 1; ok && j < it.n_kv; ++j) ok = load_tile(it, j, false);
-            ++q_cnt;
-            // Ask for the next item once this one's copies are all issued: as late as
-            // possible, and still long before its Q_A may be loaded.
-            const uint32_t s = k % NXS, u = k / NXS;
-            if (ok && u > 0 && !warp_wait(ring.empty0 + 8 * s, (u - 1) & 1)) ok = false;
-            if (ok) {
-              if (elect_one()) request_next_cta(ring.slot0 + 16 * s, ring.full0 + 8 * s);
-              __syncwarp();
-              ++n_req;
+            const int j_req = it.n_kv - kReqAhead;
+            bool asked = false;
+            for (int j = 1; ok && j < it.n_kv; ++j) {
+              if (j == j_req) {
+                request();
+                asked = true;
+              }
+              ok = ok && load_tile(it, j, false);
             }
+            if (!asked) request();
           }
         }
         // A request still in flight must land before the CTA's shared memory is released.
@@ -678,8 +697,8 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         // Every issued copy must land before the CTA's shared memory is released
         // (immediate on the normal path, where the MMA warp already waited for them).
         bool drained = true;
-        if (q_cnt > 0 && (!warp_wait(bar(BAR_Q), (q_cnt - 1) & 1) || !warp_wait(bar(BAR_Q1), (q_cnt - 1) & 1)))
-          drained = false;
+        for (uint32_t n = q_cnt > NQB ? q_cnt - NQB : 0; n < q_cnt; ++n)
+          if (!warp_wait(bar(BAR_QF + n % NQB), (n / NQB) & 1)) drained = false;
         for (uint32_t s = 0; s < NSK && s < k_cnt; ++s)
           if (!warp_wait(bar(BAR_KF + s), ((k_cnt - 1 - s) / NSK) & 1)) drained = false;
         for (uint32_t s = 0; s < NSV && s < v_cnt; ++s)
@@ -702,15 +721,14 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         // and the two Q tiles are TILE bytes apart: slot i's descriptor is the first
         // slot's plus i * (TILE >> 4).
         constexpr uint64_t kSlot = TILE >> 4;
-        const uint64_t dq = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B) + (uint64_t)t * kSlot;
+        const uint64_t dq0 = smem_desc(sb + SM_Q, 16, 1024, kSwizzle128B);
         const uint64_t dk0 = smem_desc(sb + SM_K, 16, 1024, kSwizzle128B);
         const uint64_t dv0 = smem_desc(sb + SM_V, 16384, 1024, kSwizzle128B);
         const uint32_t d_s = tmem + COL_S + t * BN, d_o = tmem + COL_O + t * HD;
-        const uint32_t q_full = bar(t == 0 ? BAR_Q : BAR_Q1), q_empty = bar(BAR_QE + t);
         // S for global step gs (keys [64*half, 64*half + 64) of the K tile at ring position
         // kg) into S buffer gs & 1; then the K stage's release (rel arrivals) after the
         // tile's second half, and Q_t's release after the item's last step.
-        auto issue_s = [&](uint32_t gs, uint32_t kg, int half, int rel_n, bool q_done) {
+        auto issue_s = [&](uint32_t gs, uint32_t kg, uint64_t dq, int half, int rel_n, uint32_t q_empty) {
           const uint64_t b0 = dk0 + (uint64_t)(kg % NSK) * kSlot + (uint64_t)((half * BS * 128) >> 4);
           if (elect_one()) {
   #pragma unroll
@@ -719,7 +737,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
               mma_bf16_ss(d_s + (gs & 1) * BS, dq + off, b0 + off, idS, k > 0);
             }
             mma_commit(bar(BAR_SF + 2 * t + (gs & 1)));
-            if (q_done) mma_commit(q_empty);  // the last product that reads this Q tile
+            if (q_empty) mma_commit(q_empty);  // the last product that reads this Q tile
             for (int i = 0; i < rel_n; ++i) mma_commit(bar(BAR_KE + kg % NSK));
           }
           __syncwarp();
@@ -740,7 +758,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           }
           __syncwarp();
         };
-        uint32_t k_cnt = 0, v_cnt = 0, q_cnt = 0, g = 0, of_cnt = 0, of_need = 0, vz_cnt = 0;
+        uint32_t k_cnt = 0, v_cnt = 0, g = 0, of_cnt = 0, of_need = 0, vz_cnt = 0;
         bool ok = true;
         uint32_t k = 0;
         for (int id = blockIdx.x; ok && id < n_items; id = next_item(ring, k++, n_items, a.err_flag)) {
@@ -752,25 +770,31 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
           // read stage j (j >= n_o), this issuer brings both arrivals, so a stage is never
           // handed back to TMA while a product of either tile may still read it.
           auto rel = [&](int j) { return j < n_o ? 1 : 2; };
+          // This item's Q tile n = 2k + t: buffer n % NQ, barriers n % NQB.
+          const uint32_t qn = 2 * k + t;
+          const uint32_t q_full = bar(BAR_QF + qn % NQB), q_empty = bar(BAR_QE + qn % NQB);
+          const uint64_t dq = dq0 + (uint64_t)(qn % NQ) * kSlot;
+          if (!warp_wait(q_full, (qn / NQB) & 1)) {
+            ok = false;
+            break;
+          }
           if (n_t == 0) {  // only B can be missing: A covers the K/V arrivals
             if (elect_one()) mma_commit(q_empty);  // its Q_B (never read) may be replaced
             __syncwarp();
             k_cnt += n_kv;
             v_cnt += n_kv;
-            ++q_cnt;
             continue;
           }
           const int n_s = 2 * n_t;  // 64-key steps
-          if (!warp_wait(q_full, q_cnt & 1) || !warp_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
+          if (!warp_wait(bar(BAR_KF + k_cnt % NSK), (k_cnt / NSK) & 1)) {
             ok = false;
             break;
           }
-          ++q_cnt;
           tc_fence_after();
           // S for the first two steps (both halves of K tile 0); the buffers were last read
           // by the previous item's last two PV products, issued earlier by this thread.
-          issue_s(g, k_cnt, 0, 0, false);
-          issue_s(g + 1, k_cnt, 1, rel(0), n_s == 2);
+          issue_s(g, k_cnt, dq, 0, 0, 0);
+          issue_s(g + 1, k_cnt, dq, 1, rel(0), n_s == 2 ? q_empty : 0);
           for (int st = 0; st < n_s; ++st, ++g) {
             const int j = st >> 1, half = st & 1;
             if (!warp_wait(bar(BAR_PF + 2 * t + (g & 1)), (g >> 1) & 1)) { ok = false; break; }
@@ -820,7 +844,7 @@ attn_tile_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
               const uint32_t kg = k_cnt + (sn >> 1);
               if ((sn & 1) == 0 && !warp_wait(bar(BAR_KF + kg % NSK), (kg / NSK) & 1)) { ok = false; break; }
               tc_fence_after();
-              issue_s(g + 2, kg, sn & 1, (sn & 1) ? rel(sn >> 1) : 0, sn == n_s - 1);
+              issue_s(g + 2, kg, dq, sn & 1, (sn & 1) ? rel(sn >> 1) : 0, sn == n_s - 1 ? q_empty : 0);
             }
           }
           k_cnt += n_kv;
