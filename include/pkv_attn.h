@@ -167,11 +167,12 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
  *   attn_decode_workspace_size(...) > PKV_NOALLOC_SCRATCH_BYTES. Fewer splits
  *   (num_splits) or a smaller batch fit.
  * - The first call on a device looks up the scratch array's device address
- *   (cudaGetSymbolAddress) with that device current, and caches it. Make that
- *   first call before any stream capture on that device. cudaDeviceReset
- *   destroys the array with the device's context, and the cached address then
- *   no longer points at it: a process that resets a device must not call this
- *   entry point on that device afterwards.
+ *   (cudaGetSymbolAddress) with that device current, and caches it with the
+ *   unique id of the current context (cuCtxGetId). Make that first call before
+ *   any stream capture on that device. cudaDeviceReset destroys the array with
+ *   the device's context; the first call in the context that replaces it sees
+ *   another context id and looks the address up again (again outside a
+ *   capture). Where the driver gives no context id, every call looks it up.
  * - Every call on a device shares the one array. Calls whose kernels overlap on
  *   the GPU (different streams, no ordering between them) race on it and give
  *   wrong results; order them, e.g. on one stream. The array keeps the last

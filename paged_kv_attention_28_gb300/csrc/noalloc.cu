@@ -1,6 +1,8 @@
 // attn_decode_paged_noalloc: paged decode whose split partial states live in a
 // fixed scratch array that belongs to the library. The caller passes no workspace,
 // and the call allocates no device memory.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -13,23 +15,63 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
 // Host code cannot use g_decode_scratch directly: in host code that name is a
-// host-side stand-in, not a device address. The device address is looked up once
-// per device, with that device current, and cached here.
+// host-side stand-in, not a device address. The device address is looked up with the
+// device current and cached per device together with the id of the context it belongs
+// to. A context that replaces the old one (after cudaDeviceReset, say) has another id,
+// and its module's copy of the array another address, so the lookup is made again.
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
+
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current context (false when there is none or the
+// driver does not say).
+bool current_context_id(unsigned long long* id) {
+  static const PfnCtxGetCurrent get_current = []() -> PfnCtxGetCurrent {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<PfnCtxGetCurrent>(p)
+               : nullptr;
+  }();
+  static const PfnCtxGetId get_id = []() -> PfnCtxGetId {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                   q == cudaDriverEntryPointSuccess
+               ? reinterpret_cast<PfnCtxGetId>(p)
+               : nullptr;
+  }();
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_DEVICE;
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchSlot& slot = g_scratch[dev];
+  if (!have_id || !slot.ptr || slot.ctx_id != id) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || !p) return check_launch(e == cudaSuccess ? cudaErrorInvalidSymbol : e);
-    g_scratch_ptr[dev] = p;
+    // Without a context id the address is not kept: it is looked up on every call.
+    slot.ptr = have_id ? p : nullptr;
+    slot.ctx_id = id;
+    *out = p;
+    return PKV_OK;
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return PKV_OK;
 }
 

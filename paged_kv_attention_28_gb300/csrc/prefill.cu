@@ -17,8 +17,8 @@
 // the two tiles' products and softmaxes overlap.
 //
 // Warp roles (512 threads, four warpgroups):
-//   warpgroup 0: warp 0 TMA producer of Q_A, Q_B (per item) and K tiles (3-stage ring;
-//                owns TMEM), warp 3 TMA producer of V tiles (2-stage ring), warps 1 and
+//   warpgroup 0: warp 0 TMA producer of Q_A, Q_B (per item) and K tiles (2-stage ring;
+//                owns TMEM), warp 3 TMA producer of V tiles (3-stage ring), warps 1 and
 //                2 MMA issuers of tiles A and B. All four run their loops as whole warps
 //                and issue from an elected lane.
 //   warpgroup 1: softmax of tile A, one thread per row (warp w reads TMEM lanes 32*(w%4)..)
