@@ -264,6 +264,45 @@ def cpu_baselines(case, budget_s=8.0):
             "sample_1core": f"{one_rate[1]} pass(es) in {one_rate[2]:.1f} s in one process"}
 
 
+def other_cpu_baselines(workloads, budget_s=3.0):
+    """The fp64 oracle, as it stands, on every host core and on one core, for the three other
+    configurations: the single-sequence fp32 decode, the long-context GQA decode and the
+    shared-prefix decode. Each leg runs whole passes over the whole workload until
+    ``budget_s`` has elapsed, after one untimed pass. GB/s of the same algorithmic bytes as
+    the GPU line."""
+    from oracle import timing
+    cores = host_cores()
+    cases = {
+        "single_seq_decode_f32": workloads.single_seq_decode_f32(),
+        "long_context_gqa_decode": workloads.long_context_gqa_decode(poison=False),
+        "cascade_shared_prefix_decode": workloads.cascade_shared_prefix_decode(poison=False),
+    }
+    res = {}
+    for name, c in cases.items():
+        def runner(workers):
+            if name == "cascade_shared_prefix_decode":
+                return timing.cascade_runner(c.q.double().numpy(), c.k_pages.float().numpy(),
+                                             c.v_pages.float().numpy(), c.prefix_table.numpy(), c.prefix_len,
+                                             c.suffix_table.numpy(), c.suffix_lens.numpy(), c.scale, workers)
+            return timing.decode_runner(c.q.double().numpy(), c.k_pages.float().numpy(),
+                                        c.v_pages.float().numpy(), c.block_table.numpy(), c.kv_lens.numpy(),
+                                        c.scale, workers)
+        legs = {}
+        for label, workers in (("all", cores), ("one", 1)):
+            r = runner(workers)
+            try:
+                passes, el = timing.time_passes(r, budget_s)
+            finally:
+                r.close()
+            legs[label] = (c.kv_bytes() * passes / el / 1e9, passes, el)
+        res[name] = {"value": legs["all"][0], "unit": "GB/s", "cores": cores, "kind": "oracle",
+                     "sample": f"{legs['all'][1]} whole pass(es) of the fp64 oracle over the full workload in "
+                               f"{legs['all'][2]:.1f} s on {cores} worker processes, after one untimed pass",
+                     "value_1core": legs["one"][0],
+                     "sample_1core": f"{legs['one'][1]} pass(es) in {legs['one'][2]:.1f} s in one process"}
+    return res
+
+
 def prefill_cpu_baseline(case):
     cores = host_cores()
     tf_all, s_all = oracle_prefill_rate(case, cores)
@@ -518,6 +557,10 @@ def run_ours(args, rank, world, local):
         line["cpu_baseline"] = cpu_baselines(case)
         if pre is not None:
             pre["cpu_baseline"] = prefill_cpu_baseline(workloads.causal_prefill_llama7b())
+        if "also" in line:
+            for name, cb in other_cpu_baselines(workloads).items():
+                if name in line["also"]:
+                    line["also"][name]["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -2,7 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY: the CPU-baseline leg of ``bench.py`` is the one user. It
 runs the oracle functions of ``oracle/attention.py`` unchanged, over independent
-units of work ((sequence, KV head) for decode, (batch, head) for prefill), either in
+units of work ((sequence, KV head) for decode, (batch, head) for prefill, a request for
+the shared-prefix decode), either in
 this process (one core) or spread over worker processes started with ``spawn``, each
 with one BLAS thread. The inputs are placed once in shared memory, so the workers
 read them without a copy. Nothing here changes what the oracle computes or how.
@@ -58,6 +59,14 @@ def _prefill_units(units):
     for b, h in units:
         _att.prefill_causal(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, h // G:h // G + 1],
                             v[b:b + 1, :, h // G:h // G + 1], _W["scale"])
+    return len(units)
+
+
+def _cascade_units(units):
+    q, kp, vp = _W["q"], _W["k_pages"], _W["v_pages"]
+    for r in units:
+        _att.cascade_decode(q[r:r + 1], kp, vp, _W["prefix_table"], _W["prefix_len"],
+                            _W["suffix_table"][r:r + 1], _W["suffix_lens"][r:r + 1], _W["scale"])
     return len(units)
 
 
@@ -134,3 +143,17 @@ def prefill_runner(q, k, v, scale, workers):
     units = [(b, h) for b in range(B) for h in range(Hq)]
     arrays = dict(q=np.asarray(q, np.float32), k=np.asarray(k, np.float32), v=np.asarray(v, np.float32))
     return _Runner(_prefill_units, arrays, {"scale": float(scale)}, units, [1.0] * len(units), workers)
+
+
+def cascade_runner(q, k_pages, v_pages, prefix_table, prefix_len, suffix_table, suffix_lens, scale,
+                   workers):
+    """The shared-prefix decode oracle over every request (each call attends the prefix and
+    the request's suffix for all of its heads)."""
+    R = q.shape[0]
+    units = list(range(R))
+    weights = [float(prefix_len + suffix_lens[r]) for r in units]
+    arrays = dict(q=np.asarray(q, np.float64), k_pages=np.asarray(k_pages, np.float32),
+                  v_pages=np.asarray(v_pages, np.float32), prefix_table=np.asarray(prefix_table, np.int32),
+                  suffix_table=np.asarray(suffix_table, np.int32), suffix_lens=np.asarray(suffix_lens, np.int32))
+    return _Runner(_cascade_units, arrays, {"scale": float(scale), "prefix_len": int(prefix_len)}, units,
+                   weights, workers)
