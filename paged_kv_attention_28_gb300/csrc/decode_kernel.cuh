@@ -75,8 +75,11 @@ struct DecodeCfg {
   static constexpr int WPH = NW / HPC;             // consumer warps per KV head
   // bf16 with one query head per KV head: a 4-stage ring and five CTAs per SM keep more
   // pages in flight per SM than 8 stages and three CTAs (measured 6359 against 6259 GB/s
-  // on the Llama-7B batch; 4 stages and four CTAs 6012).
-  static constexpr int NSTAGE = (G == 1 && sizeof(T) == 2) ? 4 : 8;  // multiple of NW
+  // on the Llama-7B batch; 4 stages and four CTAs 6012). fp32 at head_dim 64 with one query
+  // head per KV head (4 KiB tiles, few CTAs): 16 stages, so that a 256-token sequence's
+  // pages are all requested at once (32 such calls back to back: 194 against 206 us).
+  static constexpr int NSTAGE =
+      (G == 1 && sizeof(T) == 2) ? 4 : (G == 1 && sizeof(T) == 4 && D == 64 && !FP8) ? 16 : 8;  // multiple of NW
   static constexpr int THREADS = (NW + 1) * 32;
   // G = 8 (fp32, head_dim 64 and FP8: the bf16 head_dim-128 groups of 4 and 8 run on the
   // tensor cores) asks for no occupancy, and fp32 G = 4 at head_dim 128 for two CTAs per
