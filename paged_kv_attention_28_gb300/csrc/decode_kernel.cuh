@@ -289,6 +289,15 @@ decode_paged_kernel(const DecodeArgs a) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int kv_len = __ldg(a.kv_lens + b);
+  // The split's first 32 table entries are requested together with the length (their
+  // addresses do not depend on it), so the page copies wait for one round trip, not two.
+  // Entries past the sequence's end are read but never used; all lie inside the table.
+  int phys_first = 0;
+  if (warp == C::NW) {
+    const int idx = split * a.pages_per_split + lane;
+    if (lane < a.pages_per_split && idx < a.max_blocks)
+      phys_first = __ldg(a.block_table + (size_t)b * a.max_blocks + idx);
+  }
   if (kv_len < 0 || kv_len > a.max_blocks * P) {
     if (split == 0) {
       if (threadIdx.x == 0) set_err(a.err_flag, PKV_DEVERR_BAD_LEN);
@@ -336,7 +345,7 @@ decode_paged_kernel(const DecodeArgs a) {
     int issued = 0;
     for (int base = 0; base < n_pages && ok; base += 32) {
       const int idx = base + lane;
-      const int phys = (idx < n_pages) ? __ldg(trow + idx) : 0;
+      const int phys = (idx < n_pages) ? (base == 0 ? phys_first : __ldg(trow + idx)) : 0;
       const bool bad = (idx < n_pages) && (phys < 0 || phys >= a.num_pages);
       const unsigned badm = __ballot_sync(0xffffffffu, bad);
       if (badm && lane == 0) {
