@@ -579,6 +579,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
   int* hist = reinterpret_cast<int*>(smem + L::SM_HIST);
   uint16_t* ord_s = reinterpret_cast<uint16_t*>(smem + L::SM_ORD);
   const int my_bucket = lpt && threadIdx.x < a.batch ? lpt_bucket(a, threadIdx.x) : 0;
+  // Without the longest-first order a CTA's first unit is its own index, so the producers
+  // request that unit's first 32 table entries now, beside the length reads: its first
+  // copies then wait for one round trip to memory, not two. Entries past the split's pages
+  // are read but never used; all lie inside the table.
+  int ent_first = 0;
+  if (!FP8 && !lpt && (warp == 0 || warp == 2)) {
+    const int split0 = (int)blockIdx.x % a.num_splits;
+    const int b0 = (int)blockIdx.x / a.num_splits / a.n_kv_heads;
+    const int idx = split0 * a.pages_per_split + lane;
+    if (b0 < a.batch && lane < a.pages_per_split && idx < a.max_blocks)
+      ent_first = __ldg(a.block_table + (size_t)b0 * a.max_blocks + idx);
+  }
   if (lpt && threadIdx.x < LPT_BUCKETS) hist[threadIdx.x] = 0;
 
   if (threadIdx.x == 0) {
@@ -700,7 +712,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
       const int32_t* trow = a.block_table + (size_t)u.b * a.max_blocks + u.first;
       int ent = 0;
       for (int j = 0; ok && j < u.n_tiles; ++j, ++cnt) {
-        if ((j & 3) == 0) ent = (32 * (j >> 2) + lane < u.n_pages) ? __ldg(trow + 32 * (j >> 2) + lane) : 0;
+        if ((j & 3) == 0)
+          ent = (32 * (j >> 2) + lane < u.n_pages)
+                    ? ((k == 0 && j == 0 && !lpt) ? ent_first : __ldg(trow + 32 * (j >> 2) + lane))
+                    : 0;
         const uint32_t s = cnt % L::NSK, use = cnt / L::NSK;
         const uint32_t full = bar((v_role ? B_VF : B_KF) + s);
         if (use > 0 && !warp_wait(bar((v_role ? B_VE : B_KE) + s), (use - 1) & 1, lim)) {
