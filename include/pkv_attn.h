@@ -28,6 +28,9 @@
  *   means nothing was enqueued, except PKV_ERR_LAUNCH, which reports the CUDA
  *   launch error. Arguments are checked on the host before any launch. No call
  *   aborts the process.
+ * - Every compute call runs inside an NVTX range named after it (for example
+ *   "attn_decode_paged"), so that Nsight Systems or `ncu --nvtx` can attribute
+ *   kernels to calls; without a tool attached a range costs a pointer test.
  * - err_flag (nullable, int32 in device memory) collects problems that only
  *   the device can see, as a bitwise OR of PKV_DEVERR_* bits: a block-table
  *   entry outside [0, num_pages), a length above the table's capacity, or a

@@ -3,9 +3,21 @@
 #include <cmath>
 #include <cstdint>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 
 namespace pkv {
+
+// An NVTX range around each compute call, named after the call, so that a trace (Nsight
+// Systems, or ncu with --nvtx) shows which library call launched which kernels. Without a
+// tool attached an NVTX call only tests a function pointer.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 static thread_local cudaError_t g_last_error = cudaSuccess;
 
@@ -249,6 +261,7 @@ int attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
                       int n_kv_heads, int head_dim, int page_size, float scale, int num_splits,
                       int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
                       void* stream) {
+  const pkv::CallRange range("attn_decode_paged");
   DecodeCall c{q, k_pages, v_pages, block_table, kv_lens, out, lse, batch, max_blocks_per_seq,
                num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, dtype,
                workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream)};
@@ -262,6 +275,7 @@ int attn_decode_paged_unified_max(const void* q, const void* k_pages, const void
                                   float scale, int num_splits, int dtype, float phi,
                                   int32_t* fallback_count, void* workspace,
                                   size_t workspace_bytes, int32_t* err_flag, void* stream) {
+  const pkv::CallRange range("attn_decode_paged_unified_max");
   DecodeCall c{q, k_pages, v_pages, block_table, kv_lens, out, lse, batch, max_blocks_per_seq,
                num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, dtype,
                workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream)};
@@ -275,6 +289,7 @@ int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_page
                           int head_dim, int page_size, float scale, int num_splits,
                           void* workspace, size_t workspace_bytes, int32_t* err_flag,
                           void* stream) {
+  const pkv::CallRange range("attn_decode_paged_fp8");
   DecodeCall c{q, k_pages, v_pages, block_table, kv_lens, out, lse, batch, max_blocks_per_seq,
                num_pages, n_qo_heads, n_kv_heads, head_dim, page_size, scale, num_splits, PKV_BF16,
                workspace, workspace_bytes, err_flag, static_cast<cudaStream_t>(stream), k_scale,
@@ -285,6 +300,7 @@ int attn_decode_paged_fp8(const void* q, const void* k_pages, const void* v_page
 int attn_merge_states(const float* out_a, const float* lse_a, const float* out_b,
                       const float* lse_b, void* out, float* lse, int n_rows, int head_dim,
                       int out_dtype, void* stream) {
+  const pkv::CallRange range("attn_merge_states");
   if (n_rows < 0 || head_dim < 1) return PKV_ERR_INVALID_ARG;
   if (out_dtype != PKV_F32 && out_dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   if (n_rows == 0) return PKV_OK;
@@ -297,6 +313,7 @@ int attn_merge_states(const float* out_a, const float* lse_a, const float* out_b
 int attn_prefill_causal(const void* q, const void* k, const void* v, void* out, float* lse,
                         int batch, int seq_len, int n_qo_heads, int n_kv_heads, int head_dim,
                         float scale, int dtype, int32_t* err_flag, void* stream) {
+  const pkv::CallRange range("attn_prefill_causal");
   if (batch < 0 || seq_len < 0 || n_qo_heads < 1 || n_kv_heads < 1 || head_dim < 1)
     return PKV_ERR_INVALID_ARG;
   if (n_qo_heads % n_kv_heads || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
@@ -315,6 +332,7 @@ int attn_prefill_paged_chunk(const void* q, const void* k_pages, const void* v_p
                              int num_pages, int n_qo_heads, int n_kv_heads, int head_dim,
                              int page_size, float scale, int dtype, int32_t* err_flag,
                              void* stream) {
+  const pkv::CallRange range("attn_prefill_paged_chunk");
   if (batch < 0 || chunk_len < 0 || max_blocks_per_seq < 1 || num_pages < 1 || n_qo_heads < 1 ||
       n_kv_heads < 1 || head_dim < 1 || page_size < 1)
     return PKV_ERR_INVALID_ARG;
@@ -354,6 +372,7 @@ int attn_decode_cascade(const void* q, const void* k_pages, const void* v_pages,
                         int n_qo_heads, int n_kv_heads, int head_dim, int page_size, float scale,
                         int dtype, void* workspace, size_t workspace_bytes, int32_t* err_flag,
                         void* stream) {
+  const pkv::CallRange range("attn_decode_cascade");
   if (n_requests < 0 || prefix_len < 0 || max_suffix_blocks < 1 || num_pages < 1 ||
       n_qo_heads < 1 || n_kv_heads < 1 || head_dim < 1 || page_size < 1)
     return PKV_ERR_INVALID_ARG;
@@ -424,6 +443,7 @@ int attn_flat_gemm_num_splits(int m, int n, int k) {
 
 int attn_flat_gemm(const void* x, const void* w, void* y, int m, int n, int k, int dtype,
                    int32_t* err_flag, void* stream) {
+  const pkv::CallRange range("attn_flat_gemm");
   if (m < 0 || n < 0 || k < 1) return PKV_ERR_INVALID_ARG;
   if (dtype != PKV_F32 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
   if (m == 0 || n == 0) return PKV_OK;
