@@ -179,9 +179,13 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         sm = [r[1] for r in used]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": used[-1][2] if used else None, "reasons": sorted(reasons),
-                "samples_in_region": len(inside), "samples_used": len(used)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": used[-1][2] if used else None, "reasons": sorted(reasons),
+               "samples_in_region": len(inside), "samples_used": len(used)}
+        if not inside and used:
+            out["note"] = ("the timed region is shorter than the 100 ms sampling period: the nearest "
+                           "sample on each side, both taken while the same step ran back to back")
+        return out
 
 
 def dist_init():
